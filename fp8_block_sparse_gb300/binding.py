@@ -1,0 +1,218 @@
+"""ctypes binding of libmsa.so (declared in include/msa.h).
+
+Argument marshalling only: tensors become device pointers, optional scales
+become host float pointers (None -> NULL = unit scale), the current torch
+stream becomes the launch stream. Every step of the path runs in the
+library's CUDA kernels; when the library is missing, every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB: Optional[ctypes.CDLL] = None
+
+MSA_BF16, MSA_FP16, MSA_E4M3, MSA_E5M2 = 0, 1, 2, 3
+_STATUS = {0: "MSA_OK", 1: "MSA_ERR_INVALID_ARG", 2: "MSA_ERR_UNSUPPORTED", 3: "MSA_ERR_CUDA",
+           4: "MSA_ERR_TIMEOUT", 5: "MSA_ERR_WORKSPACE", 6: "MSA_ERR_DATA"}
+
+
+class MsaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+def lib_path() -> str:
+    return os.path.join(_HERE, "libmsa.so")
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_I64 = ctypes.c_int64
+_F = ctypes.c_float
+_FP = ctypes.POINTER(ctypes.c_float)
+_SZ = ctypes.c_size_t
+
+_SIGNATURES = {
+    "msa_version": ([], _I),
+    "msa_last_error_string": ([], ctypes.c_char_p),
+    "msa_check_errors": ([_P], _I),
+    "msa_quant_fp8": ([_P, _I, _I64, _I64, _I64, _P, _I, _I64, _FP, _P], _I),
+    "msa_index_topk_workspace_size": ([_I, _I, _I], _SZ),
+    "msa_index_topk": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P], _I),
+    "msa_sparse_attn_workspace_size": ([_I, _I, _I, _I, _I, _I], _SZ),
+    "msa_sparse_attn_fwd": ([_P, _P, _P, _P, _P, _P, _P, _P, _F, _FP, _FP, _FP,
+                             _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _SZ, _P], _I),
+    "msa_sparse_mla_fwd": ([_P, _P, _P, _P, _P, _F, _FP, _FP, _I, _I, _I, _I, _I, _I,
+                            _P, _P, _P, _P], _I),
+}
+
+
+def load(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load the library (once). Raises when it has not been built."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    p = path or lib_path()
+    if not os.path.exists(p):
+        raise MsaError(3, f"{p} is missing; build it with __graft_entry__.build()")
+    lib = ctypes.CDLL(p)
+    for name, (args, res) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    _LIB = lib
+    return lib
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        msg = load().msa_last_error_string()
+        raise MsaError(status, msg.decode() if msg else "")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _scale(s: Optional[float]):
+    return None if s is None else ctypes.pointer(ctypes.c_float(float(s)))
+
+
+def _stream(stream: Optional[torch.cuda.Stream]):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None) -> None:
+    if not t.is_cuda:
+        raise MsaError(1, f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise MsaError(1, f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise MsaError(1, f"{name} must be contiguous")
+
+
+def check_errors(stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Synchronise and raise if a kernel recorded a device-side data error."""
+    _check(load().msa_check_errors(_stream(stream)))
+
+
+def quant_fp8(x: torch.Tensor, scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+              stream=None) -> torch.Tensor:
+    """e4m3 codes of x * (1/scale) (step a1); x is bf16 or fp16, last dim contiguous."""
+    lib = load()
+    if x.dtype not in (torch.bfloat16, torch.float16):
+        raise MsaError(1, f"x must be bf16 or fp16, got {x.dtype}")
+    if x.stride(-1) != 1:
+        raise MsaError(1, "x must have a contiguous last dimension")
+    cols = x.shape[-1]
+    rows = x.numel() // cols if cols else 0
+    x2 = x.reshape(rows, cols) if x.dim() != 2 else x
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    o2 = out.view(rows, cols)
+    _check(lib.msa_quant_fp8(_ptr(x2), MSA_BF16 if x.dtype == torch.bfloat16 else MSA_FP16,
+                             rows, cols, x2.stride(0) if rows else cols, _ptr(o2), MSA_E4M3,
+                             o2.stride(0) if rows else cols, _scale(scale), _stream(stream)))
+    return out
+
+
+def index_topk_workspace_size(T: int, Hidx: int, max_pages: int) -> int:
+    return int(load().msa_index_topk_workspace_size(T, Hidx, max_pages))
+
+
+def index_topk(idx_q: torch.Tensor, idx_k_cache: torch.Tensor, page_table: torch.Tensor,
+               seq_lens: torch.Tensor, cu_q: torch.Tensor, topk: int, max_q_len: int,
+               out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+               stream=None) -> torch.Tensor:
+    """topk_indices [Hidx, T, topk] int32 (steps a2+a3)."""
+    lib = load()
+    T, Hidx, D = idx_q.shape
+    num_pages = idx_k_cache.shape[0]
+    B, max_pages = page_table.shape
+    for t, n in ((idx_q, "idx_q"), (idx_k_cache, "idx_k_cache")):
+        _dev(t, n, torch.uint8)
+    for t, n in ((page_table, "page_table"), (seq_lens, "seq_lens"), (cu_q, "cu_q")):
+        _dev(t, n, torch.int32)
+    if out is None:
+        out = torch.empty((Hidx, T, topk), dtype=torch.int32, device=idx_q.device)
+    ws_bytes = index_topk_workspace_size(T, Hidx, max_pages)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=idx_q.device)
+    _check(lib.msa_index_topk(_ptr(idx_q), _ptr(idx_k_cache), _ptr(page_table), _ptr(seq_lens),
+                              _ptr(cu_q), B, T, max_q_len, Hidx, D, topk, num_pages, max_pages,
+                              _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out
+
+
+def sparse_attn_workspace_size(B: int, T: int, max_q_len: int, Hkv: int, D: int, max_pages: int) -> int:
+    return int(load().msa_sparse_attn_workspace_size(B, T, max_q_len, Hkv, D, max_pages))
+
+
+def sparse_attn_fwd(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                    page_table: torch.Tensor, seq_lens: torch.Tensor, cu_q: torch.Tensor,
+                    topk_indices: torch.Tensor, sink: Optional[torch.Tensor], sm_scale: float,
+                    q_scale: Optional[float], k_scale: Optional[float], v_scale: Optional[float],
+                    max_q_len: int, out=None, max_logit=None, lse=None, workspace=None,
+                    stream=None):
+    """Sparse GQA attention (steps a4/a5). Returns (out bf16, max_logit, lse)."""
+    lib = load()
+    T, Hq, D = q.shape
+    num_pages, Hkv = k_cache.shape[0], k_cache.shape[1]
+    Hidx, _, topk = topk_indices.shape
+    B, max_pages = page_table.shape
+    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _dev(t, n, torch.uint8)
+    for t, n in ((page_table, "page_table"), (seq_lens, "seq_lens"), (cu_q, "cu_q"),
+                 (topk_indices, "topk_indices")):
+        _dev(t, n, torch.int32)
+    if sink is not None:
+        _dev(sink, "sink", torch.float32)
+    dev = q.device
+    out = torch.empty((T, Hq, D), dtype=torch.bfloat16, device=dev) if out is None else out
+    max_logit = torch.empty((T, Hq), dtype=torch.float32, device=dev) if max_logit is None else max_logit
+    lse = torch.empty((T, Hq), dtype=torch.float32, device=dev) if lse is None else lse
+    ws_bytes = sparse_attn_workspace_size(B, T, max_q_len, Hkv, D, max_pages)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    _check(lib.msa_sparse_attn_fwd(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table), _ptr(seq_lens), _ptr(cu_q),
+        _ptr(topk_indices), _ptr(sink), float(sm_scale), _scale(q_scale), _scale(k_scale),
+        _scale(v_scale), B, T, max_q_len, Hq, Hkv, Hidx, D, topk, num_pages, max_pages,
+        _ptr(out), _ptr(max_logit), _ptr(lse), _ptr(workspace), workspace.numel(),
+        _stream(stream)))
+    return out, max_logit, lse
+
+
+def sparse_mla_fwd(q: torch.Tensor, kv: torch.Tensor, indices: torch.Tensor,
+                   topk_length: Optional[torch.Tensor], sink: Optional[torch.Tensor],
+                   sm_scale: float, q_scale: Optional[float], kv_scale: Optional[float],
+                   d_v: int = 512, out=None, max_logits=None, lse=None, stream=None):
+    """Sparse MLA prefill (step a6). Returns (out bf16, max_logits, lse)."""
+    lib = load()
+    T, H, d_qk = q.shape
+    S_kv = kv.shape[0]
+    topk = indices.shape[1]
+    _dev(q, "q", torch.uint8)
+    _dev(kv, "kv", torch.uint8)
+    _dev(indices, "indices", torch.int32)
+    if topk_length is not None:
+        _dev(topk_length, "topk_length", torch.int32)
+    if sink is not None:
+        _dev(sink, "sink", torch.float32)
+    dev = q.device
+    out = torch.empty((T, H, d_v), dtype=torch.bfloat16, device=dev) if out is None else out
+    max_logits = torch.empty((T, H), dtype=torch.float32, device=dev) if max_logits is None else max_logits
+    lse = torch.empty((T, H), dtype=torch.float32, device=dev) if lse is None else lse
+    _check(lib.msa_sparse_mla_fwd(_ptr(q), _ptr(kv), _ptr(indices), _ptr(topk_length), _ptr(sink),
+                                  float(sm_scale), _scale(q_scale), _scale(kv_scale), T, H, S_kv,
+                                  d_qk, d_v, topk, _ptr(out), _ptr(max_logits), _ptr(lse),
+                                  _stream(stream)))
+    return out, max_logits, lse

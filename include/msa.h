@@ -1,0 +1,217 @@
+/*
+ * msa.h -- C ABI of libmsa.so: FP8 (e4m3) top-k block-sparse attention on
+ * GB300 (sm_103a).
+ *
+ * The library computes the three steps of the sparse-attention hot path:
+ *   (a) per-tensor e4m3 quantisation of Q and the indexer query
+ *       -> msa_quant_fp8
+ *   (b) indexer scores reduced per 128-token block, then a strictly
+ *       ascending top-k of block ids into topk_indices[Hidx, T, topk]
+ *       -> msa_index_topk
+ *   (c) GQA sparse attention over the selected blocks with a per-head sink,
+ *       prefill and paged decode -> msa_sparse_attn_fwd; and the sparse-MLA
+ *       prefill variant over per-query token indices -> msa_sparse_mla_fwd
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Pointers named as tensors are DEVICE pointers; scale pointers
+ *   (q_scale, k_scale, ...) are HOST pointers to one float, and NULL means
+ *   unit scale (the C form of the pages' Optional[float] = None).
+ * - Every output buffer and every workspace is owned by the caller and
+ *   preallocated; the library never allocates device memory and never
+ *   synchronises the stream. Work is enqueued on `stream` (NULL = the legacy
+ *   default stream) and runs asynchronously.
+ * - Kernels overwrite every element of their outputs, so callers may pass
+ *   uninitialised buffers.
+ * - Arguments are validated on the host before anything is launched. A
+ *   failed check returns a non-zero msa_status and launches nothing;
+ *   msa_last_error_string() then describes the failure (thread-local).
+ * - Device-side data errors (a page id outside [0, num_pages), a wait that
+ *   ran out its iteration limit) never trap: the kernel skips the bad tile,
+ *   records a bit in a device error word and returns; msa_check_errors()
+ *   reports and clears it.
+ * - Layouts are row-major with the last dimension contiguous.
+ *   KV page layout: [num_pages][Hkv][128 tokens][D] e4m3; one (page, head)
+ *   tile is 16 KB contiguous. Index-K cache: [num_pages][128][d_idx] e4m3,
+ *   with no head axis (shared by all index heads).
+ * - Batch description: sequence b has seq_lens[b] tokens in its cache; its
+ *   query tokens are the LAST q_len_b = cu_q[b+1]-cu_q[b] of them, stored at
+ *   rows cu_q[b] .. cu_q[b+1]-1 of the query tensors. Prefill of one
+ *   sequence: B = 1, cu_q = {0, T}, seq_lens = {T}. Decode: q_len_b = 1.
+ *   max_q_len is the host's bound on q_len_b (1 selects the decode kernels).
+ *   page_table[b * max_pages + j] is the physical page of logical block j.
+ *
+ * Sources: the four web pages this method is described on --
+ *   [30971] sglang PR 30971 page, "M3 attention GEMMs fully fp8";
+ *   [45892] vLLM PR 45892 page, "SM100 MSA indexer backend for MiniMax M3";
+ *   [25751] sglang PR 25751 page, "SM90 Q8KV8 FP8 sparse MLA prefill kernel";
+ *   [25460] sglang PR 25460 page, "prefill QKV quantize hook and FP8 Triton
+ *           kernel".
+ */
+#ifndef MSA_H_
+#define MSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* msa_stream_t;
+
+typedef enum msa_status {
+  MSA_OK = 0,
+  MSA_ERR_INVALID_ARG = 1,  /* null pointer, bad size or stride, misalignment */
+  MSA_ERR_UNSUPPORTED = 2,  /* e5m2, head_dim / topk / page size not built */
+  MSA_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
+  MSA_ERR_TIMEOUT = 4,      /* a device wait ran out its iteration limit */
+  MSA_ERR_WORKSPACE = 5,    /* workspace pointer NULL or smaller than required */
+  MSA_ERR_DATA = 6          /* device-side data error (page id out of range) */
+} msa_status;
+
+typedef enum msa_dtype {
+  MSA_BF16 = 0,
+  MSA_FP16 = 1,
+  MSA_E4M3 = 2,
+  MSA_E5M2 = 3   /* never accepted: the e5m2 variant must not enter this path */
+} msa_dtype;
+
+/* Library version (major*10000 + minor*100 + patch). */
+int msa_version(void);
+
+/* Message describing the last non-OK status returned on this thread. */
+const char* msa_last_error_string(void);
+
+/*
+ * Synchronises `stream`, then reads and clears the device error word.
+ * Returns MSA_OK, MSA_ERR_DATA (bad page id / index seen by a kernel) or
+ * MSA_ERR_TIMEOUT (a bounded device wait gave up), or MSA_ERR_CUDA.
+ * This is the only entry point that synchronises; call it outside graph
+ * capture.
+ */
+msa_status msa_check_errors(msa_stream_t stream);
+
+/*
+ * Step (a): out[r, c] = e4m3_rn_satfinite( fp32(x[r, c]) * s_inv ),
+ * s_inv = 1.0f / *scale computed once in fp32 on the host, or 1 when scale
+ * is NULL. [25460] key source excerpt (fp8_quantize: widen, multiply by
+ * scale_inv, cast); [30971] implementation step 3 (_quant_q_fp8 on q and
+ * idx_q; a missing scale means no division).
+ *
+ * x:        device, `rows` rows of `cols` bf16 or fp16 elements, row r at
+ *           element offset r * x_row_stride (any leading dims flattened into
+ *           rows; the last dim must be contiguous).
+ * out:      device, e4m3 bytes, row r at byte offset r * out_row_stride.
+ * x_dtype:  MSA_BF16 or MSA_FP16; out_dtype must be MSA_E4M3 (MSA_E5M2
+ *           returns MSA_ERR_UNSUPPORTED; no silent reinterpretation).
+ * rows/cols may be 0 (nothing is launched). Strides are in elements, >= cols.
+ * Overflow saturates to +-448; NaN stays NaN.
+ */
+msa_status msa_quant_fp8(const void* x, msa_dtype x_dtype, int64_t rows, int64_t cols,
+                         int64_t x_row_stride, void* out, msa_dtype out_dtype,
+                         int64_t out_row_stride, const float* scale, msa_stream_t stream);
+
+/* Bytes of device workspace msa_index_topk needs for these sizes. */
+size_t msa_index_topk_workspace_size(int T, int Hidx, int max_pages);
+
+/*
+ * Step (b): block scores and the ascending top-k.
+ * For index head i and query token t at position p (own block o = p / 128):
+ *   score[i, t, j] = max over the 128 keys k of block j < o of
+ *                    dot(idx_q[t, i, :], idx_k[k, :])   (codes, fp32 accum.)
+ * topk_indices[i, t, :] = if o + 1 <= topk: 0, 1, ..., o, then -1 padding;
+ *   else: the topk-1 highest-scoring blocks j < o (equal scores: lower id
+ *   first) in ascending order, followed by o.
+ * [45892] implementation steps 1-4 (per-page max score, head-less fp8
+ * index cache, shared topk_indices_buffer [index_heads, tokens, topk]);
+ * [30971] implementation step 2 and review item 2 (strictly ascending ids,
+ * -1 padding when the causal blocks do not exceed topk). Forcing the own
+ * block and the tie order are readings of this library.
+ *
+ * idx_q:        device e4m3 [T][Hidx][D]
+ * idx_k_cache:  device e4m3 [num_pages][128][D]
+ * page_table:   device int32 [B][max_pages]
+ * seq_lens:     device int32 [B];  cu_q: device int32 [B+1]
+ * topk_indices: device int32 [Hidx][T][topk] (written in full)
+ * workspace:    device, >= msa_index_topk_workspace_size(T, Hidx, max_pages)
+ *               bytes, 256-byte aligned; contents on entry are ignored.
+ * Supported: D in {64, 128}; 1 <= topk <= 64 (topk >= 2 when blocks must be
+ * ranked); Hidx >= 1.
+ */
+msa_status msa_index_topk(const uint8_t* idx_q, const uint8_t* idx_k_cache,
+                          const int32_t* page_table, const int32_t* seq_lens,
+                          const int32_t* cu_q, int B, int T, int max_q_len, int Hidx, int D,
+                          int topk, int num_pages, int max_pages, int32_t* topk_indices,
+                          void* workspace, size_t workspace_bytes, msa_stream_t stream);
+
+/* Bytes of device workspace msa_sparse_attn_fwd needs for these sizes. */
+size_t msa_sparse_attn_workspace_size(int B, int T, int max_q_len, int Hkv, int D, int max_pages);
+
+/*
+ * Step (c): GQA sparse attention over the selected blocks.
+ * Query row (t, h) uses index head i = h / (Hq/Hidx) and kv head
+ * g = h / (Hq/Hkv); it attends to every key of the blocks listed in
+ * topk_indices[i, t, :] (ids < 0 ignored) whose position is <= its own.
+ * With c = sm_scale * q_scale:
+ *   l_j      = c * k_scale * dot(q[t,h,:], k_j)     (codes)
+ *   sigma    = c * sink[h]                          (no k_scale)
+ *   out      = v_scale * sum_j e^{l_j} v_j / (sum_j e^{l_j} + e^{sigma})
+ *   max_logit = max_j l_j;   lse = ln(sum_j e^{l_j} + e^{sigma})
+ * (no sigma terms when sink is NULL). [30971] implementation step 3 and the
+ * executive summary: q_scale folded into sm_scale acts on the dot and the
+ * sink; k_scale never touches the sink; v_scale scales the output.
+ * [45892] step 2: attention reads the topk buffer the indexer wrote.
+ *
+ * q:            device e4m3 [T][Hq][D]
+ * k_cache, v_cache: device e4m3 [num_pages][Hkv][128][D]
+ * topk_indices: device int32 [Hidx][T][topk], ascending, -1 padded
+ * sink:         device fp32 [Hq] or NULL
+ * out:          device bf16 [T][Hq][D];  max_logit, lse: device fp32 [T][Hq]
+ * workspace:    device, >= msa_sparse_attn_workspace_size(...) bytes
+ *               (0 for decode), 256-byte aligned.
+ * Supported: D == 128; Hq % Hkv == 0, Hq % Hidx == 0, Hq/Hkv a power of two
+ * <= 16; 1 <= topk <= 64.
+ */
+msa_status msa_sparse_attn_fwd(const uint8_t* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                               const int32_t* page_table, const int32_t* seq_lens,
+                               const int32_t* cu_q, const int32_t* topk_indices,
+                               const float* sink, float sm_scale, const float* q_scale,
+                               const float* k_scale, const float* v_scale, int B, int T,
+                               int max_q_len, int Hq, int Hkv, int Hidx, int D, int topk,
+                               int num_pages, int max_pages, uint16_t* out, float* max_logit,
+                               float* lse, void* workspace, size_t workspace_bytes,
+                               msa_stream_t stream);
+
+/*
+ * Step (c), sparse-MLA prefill: MQA of H query heads over one latent kv head.
+ * Query t attends to kv rows indices[t, j] for j < topk_length[t] (all topk
+ * when topk_length is NULL), skipping negative entries; V is the first d_v
+ * columns of the same rows. With c = sm_scale * q_scale:
+ *   l_j = c * kv_scale * dot(q[t,h,:], kv[idx_j, :]);  sigma = c * sink[h]
+ *   out = kv_scale * sum_j e^{l_j} kv[idx_j, :d_v] / (sum_j e^{l_j} + e^{sigma})
+ *   max_logits = max_j l_j;  lse = ln(sum_j e^{l_j} + e^{sigma})
+ * [25751] key source excerpt (sparse_mla_q8kv8_prefill_fwd: q, kv, indices,
+ * sm_scale, q_scale, kv_scale, d_v, attn_sink, topk_length; caller-owned
+ * out [s_q, h_q, d_v] bf16, max_logits and lse [s_q, h_q] fp32; d_v other
+ * than 512 is rejected).
+ *
+ * q:   device e4m3 [T][H][d_qk];  kv: device e4m3 [S_kv][d_qk]
+ * indices: device int32 [T][topk];  topk_length: device int32 [T] or NULL
+ * sink: device fp32 [H] or NULL
+ * out: device bf16 [T][H][d_v];  max_logits, lse: device fp32 [T][H]
+ * Supported: d_qk == 576, d_v == 512, H == 128, topk a multiple of 64.
+ * An index >= S_kv is a data error (recorded, key skipped).
+ */
+msa_status msa_sparse_mla_fwd(const uint8_t* q, const uint8_t* kv, const int32_t* indices,
+                              const int32_t* topk_length, const float* sink, float sm_scale,
+                              const float* q_scale, const float* kv_scale, int T, int H,
+                              int S_kv, int d_qk, int d_v, int topk, uint16_t* out,
+                              float* max_logits, float* lse, msa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MSA_H_ */
