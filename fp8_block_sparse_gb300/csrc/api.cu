@@ -1,0 +1,352 @@
+// api.cu -- the C ABI of libmsa.so (include/msa.h): argument validation,
+// scale folding, workspace checks and dispatch to the kernel launchers.
+// Nothing here allocates device memory or synchronises a stream (except
+// msa_check_errors, which exists to do exactly that).
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include <cudaTypedefs.h>
+
+#include "../../include/msa.h"
+#include "internal.h"
+
+namespace msa {
+
+__device__ unsigned g_msa_error_word;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+msa_status fail(msa_status s, const std::string& msg) {
+  g_last_error = msg;
+  return s;
+}
+
+msa_status cuda_fail(cudaError_t e, const char* where, const char* why = nullptr) {
+  std::string m = std::string(where) + ": " + cudaGetErrorString(e);
+  if (why) m += std::string(" (") + why + ")";
+  g_last_error = m;
+  return MSA_ERR_CUDA;
+}
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mutex;
+unsigned* g_err_ptr[kMaxDevices] = {};
+int g_sms[kMaxDevices] = {};
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int current_device() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return -1;
+  return d;
+}
+
+bool aligned(const void* p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
+
+// A missing scale is the unit scale; a given one must be finite and positive.
+bool read_scale(const float* s, float* out, const char* name) {
+  if (s == nullptr) {
+    *out = 1.0f;
+    return true;
+  }
+  if (!std::isfinite(*s) || !(*s > 0.0f)) {
+    g_last_error = std::string(name) + " must be finite and > 0";
+    return false;
+  }
+  *out = *s;
+  return true;
+}
+
+}  // namespace
+
+unsigned* device_error_word() {
+  const int d = current_device();
+  if (d < 0) return nullptr;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (g_err_ptr[d] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_msa_error_word) != cudaSuccess) return nullptr;
+    g_err_ptr[d] = static_cast<unsigned*>(p);
+  }
+  return g_err_ptr[d];
+}
+
+int num_sms() {
+  const int d = current_device();
+  if (d < 0) return 148;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (g_sms[d] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d);
+    g_sms[d] = n > 0 ? n : 148;
+  }
+  return g_sms[d];
+}
+
+bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base,
+                       const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                       CUtensorMapSwizzle swizzle, const char** why) {
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (g_encode == nullptr) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr) {
+        *why = "cuTensorMapEncodeTiled entry point unavailable";
+        return false;
+      }
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+  }
+  cuuint64_t d[5], s[4];
+  cuuint32_t b[5], e[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+    e[i] = 1;
+    if (i + 1 < rank) s[i] = strides_bytes[i];
+  }
+  std::memset(map, 0, sizeof(*map));
+  CUresult r = g_encode(map, dtype, rank, const_cast<void*>(base), d, s, b, e,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    *why = "cuTensorMapEncodeTiled rejected the tensor (alignment or extent)";
+    return false;
+  }
+  return true;
+}
+
+}  // namespace msa
+
+using namespace msa;
+
+extern "C" {
+
+int msa_version(void) { return 100; }
+
+const char* msa_last_error_string(void) { return g_last_error.c_str(); }
+
+msa_status msa_check_errors(msa_stream_t stream) {
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "msa_check_errors");
+  unsigned* p = device_error_word();
+  if (p == nullptr) return fail(MSA_ERR_CUDA, "msa_check_errors: no device error word");
+  unsigned word = 0;
+  e = cudaMemcpy(&word, p, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "msa_check_errors");
+  e = cudaMemset(p, 0, sizeof(unsigned));
+  if (e != cudaSuccess) return cuda_fail(e, "msa_check_errors");
+  if (word & MSA_DEVERR_TIMEOUT) return fail(MSA_ERR_TIMEOUT, "a device wait ran out its limit");
+  if (word & MSA_DEVERR_DATA)
+    return fail(MSA_ERR_DATA, "a kernel saw a page id or index outside its valid range");
+  return MSA_OK;
+}
+
+msa_status msa_quant_fp8(const void* x, msa_dtype x_dtype, int64_t rows, int64_t cols,
+                         int64_t x_row_stride, void* out, msa_dtype out_dtype,
+                         int64_t out_row_stride, const float* scale, msa_stream_t stream) {
+  if (out_dtype == MSA_E5M2)
+    return fail(MSA_ERR_UNSUPPORTED, "msa_quant_fp8: e5m2 output is not supported (e4m3 only)");
+  if (out_dtype != MSA_E4M3) return fail(MSA_ERR_INVALID_ARG, "msa_quant_fp8: out_dtype must be MSA_E4M3");
+  if (x_dtype != MSA_BF16 && x_dtype != MSA_FP16)
+    return fail(MSA_ERR_INVALID_ARG, "msa_quant_fp8: x_dtype must be MSA_BF16 or MSA_FP16");
+  if (rows < 0 || cols < 0) return fail(MSA_ERR_INVALID_ARG, "msa_quant_fp8: negative size");
+  float s = 1.0f;
+  if (!read_scale(scale, &s, "msa_quant_fp8: scale")) return MSA_ERR_INVALID_ARG;
+  if (rows == 0 || cols == 0) return MSA_OK;
+  if (x == nullptr || out == nullptr) return fail(MSA_ERR_INVALID_ARG, "msa_quant_fp8: null pointer");
+  if (x_row_stride < cols || out_row_stride < cols)
+    return fail(MSA_ERR_INVALID_ARG, "msa_quant_fp8: row stride smaller than cols");
+  if (!aligned(x, 2)) return fail(MSA_ERR_INVALID_ARG, "msa_quant_fp8: x not 2-byte aligned");
+  const float s_inv = (scale == nullptr) ? 1.0f : 1.0f / s;
+  cudaError_t e = launch_quant(x, x_dtype == MSA_BF16, rows, cols, x_row_stride,
+                               static_cast<uint8_t*>(out), out_row_stride, s_inv,
+                               reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "msa_quant_fp8");
+  return MSA_OK;
+}
+
+size_t msa_index_topk_workspace_size(int T, int Hidx, int max_pages) {
+  if (T < 0 || Hidx < 0 || max_pages < 0) return 0;
+  return index_workspace_bytes(T, Hidx, max_pages);
+}
+
+msa_status msa_index_topk(const uint8_t* idx_q, const uint8_t* idx_k_cache,
+                          const int32_t* page_table, const int32_t* seq_lens, const int32_t* cu_q,
+                          int B, int T, int max_q_len, int Hidx, int D, int topk, int num_pages,
+                          int max_pages, int32_t* topk_indices, void* workspace,
+                          size_t workspace_bytes, msa_stream_t stream) {
+  const char* fn = "msa_index_topk";
+  if (B < 1 || T < 0 || Hidx < 1 || num_pages < 1 || max_pages < 1)
+    return fail(MSA_ERR_INVALID_ARG, std::string(fn) + ": bad B/T/Hidx/num_pages/max_pages");
+  if (max_q_len < 1 || (T > 0 && max_q_len > T))
+    return fail(MSA_ERR_INVALID_ARG, std::string(fn) + ": max_q_len must be in [1, T]");
+  if (D != 64 && D != 128)
+    return fail(MSA_ERR_UNSUPPORTED, std::string(fn) + ": index head dim must be 64 or 128");
+  if (topk < 1 || topk > 64)
+    return fail(MSA_ERR_UNSUPPORTED, std::string(fn) + ": topk must be in [1, 64]");
+  if (T == 0) return MSA_OK;
+  if (!idx_q || !idx_k_cache || !page_table || !seq_lens || !cu_q || !topk_indices)
+    return fail(MSA_ERR_INVALID_ARG, std::string(fn) + ": null pointer");
+  if (!aligned(idx_q, 16) || !aligned(idx_k_cache, 16))
+    return fail(MSA_ERR_INVALID_ARG, std::string(fn) + ": idx_q / idx_k_cache must be 16-byte aligned");
+  const size_t need = index_workspace_bytes(T, Hidx, max_pages);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256)))
+    return fail(MSA_ERR_WORKSPACE, std::string(fn) + ": workspace missing, too small or not 256-byte aligned (need " +
+                                       std::to_string(need) + " bytes)");
+  IndexArgs a{};
+  a.idx_q = idx_q;
+  a.idx_k = idx_k_cache;
+  a.page_table = page_table;
+  a.seq_lens = seq_lens;
+  a.cu_q = cu_q;
+  a.B = B;
+  a.T = T;
+  a.max_q_len = max_q_len;
+  a.Hidx = Hidx;
+  a.D = D;
+  a.topk = topk;
+  a.num_pages = num_pages;
+  a.max_pages = max_pages;
+  a.topk_indices = topk_indices;
+  a.scores = static_cast<float*>(workspace);
+  a.err = device_error_word();
+  if (a.err == nullptr) return fail(MSA_ERR_CUDA, std::string(fn) + ": no device error word");
+  const char* why = nullptr;
+  cudaError_t e = launch_index_topk(a, reinterpret_cast<cudaStream_t>(stream), &why);
+  if (e != cudaSuccess) return cuda_fail(e, fn, why);
+  return MSA_OK;
+}
+
+size_t msa_sparse_attn_workspace_size(int B, int T, int max_q_len, int Hkv, int D, int max_pages) {
+  if (B < 0 || T < 0 || max_q_len < 0 || Hkv < 0 || D < 0 || max_pages < 0) return 0;
+  return attn_workspace_bytes(B, T, max_q_len, Hkv, D, max_pages);
+}
+
+msa_status msa_sparse_attn_fwd(const uint8_t* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                               const int32_t* page_table, const int32_t* seq_lens,
+                               const int32_t* cu_q, const int32_t* topk_indices, const float* sink,
+                               float sm_scale, const float* q_scale, const float* k_scale,
+                               const float* v_scale, int B, int T, int max_q_len, int Hq, int Hkv,
+                               int Hidx, int D, int topk, int num_pages, int max_pages,
+                               uint16_t* out, float* max_logit, float* lse, void* workspace,
+                               size_t workspace_bytes, msa_stream_t stream) {
+  const char* fn = "msa_sparse_attn_fwd";
+  if (B < 1 || T < 0 || Hq < 1 || Hkv < 1 || Hidx < 1 || num_pages < 1 || max_pages < 1)
+    return fail(MSA_ERR_INVALID_ARG, std::string(fn) + ": bad sizes");
+  if (max_q_len < 1 || (T > 0 && max_q_len > T))
+    return fail(MSA_ERR_INVALID_ARG, std::string(fn) + ": max_q_len must be in [1, T]");
+  if (Hq % Hkv != 0 || Hq % Hidx != 0)
+    return fail(MSA_ERR_INVALID_ARG, std::string(fn) + ": Hq must be a multiple of Hkv and of Hidx");
+  const int group = Hq / Hkv;
+  if (group > 16 || (group & (group - 1)) != 0)
+    return fail(MSA_ERR_UNSUPPORTED, std::string(fn) + ": Hq/Hkv must be a power of two <= 16");
+  if (D != 128) return fail(MSA_ERR_UNSUPPORTED, std::string(fn) + ": head_dim must be 128");
+  if (topk < 1 || topk > 64) return fail(MSA_ERR_UNSUPPORTED, std::string(fn) + ": topk must be in [1, 64]");
+  if (!std::isfinite(sm_scale) || !(sm_scale > 0.0f))
+    return fail(MSA_ERR_INVALID_ARG, std::string(fn) + ": sm_scale must be finite and > 0");
+  float qs, ks, vs;
+  if (!read_scale(q_scale, &qs, "q_scale") || !read_scale(k_scale, &ks, "k_scale") ||
+      !read_scale(v_scale, &vs, "v_scale"))
+    return MSA_ERR_INVALID_ARG;
+  if (T == 0) return MSA_OK;
+  if (!q || !k_cache || !v_cache || !page_table || !seq_lens || !cu_q || !topk_indices || !out ||
+      !max_logit || !lse)
+    return fail(MSA_ERR_INVALID_ARG, std::string(fn) + ": null pointer");
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
+    return fail(MSA_ERR_INVALID_ARG, std::string(fn) + ": q/k/v/out must be 16-byte aligned");
+  const size_t need = attn_workspace_bytes(B, T, max_q_len, Hkv, D, max_pages);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256)))
+    return fail(MSA_ERR_WORKSPACE, std::string(fn) + ": workspace missing, too small or not 256-byte aligned (need " +
+                                       std::to_string(need) + " bytes)");
+  AttnArgs a{};
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.page_table = page_table;
+  a.seq_lens = seq_lens;
+  a.cu_q = cu_q;
+  a.topk = topk_indices;
+  a.sink = sink;
+  a.c_sink = sm_scale * qs;   // q_scale folded into sm_scale: acts on the dot and the sink
+  a.c_qk = a.c_sink * ks;     // k_scale on the dot only
+  a.v_scale = vs;
+  a.B = B;
+  a.T = T;
+  a.max_q_len = max_q_len;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.Hidx = Hidx;
+  a.D = D;
+  a.topk_k = topk;
+  a.num_pages = num_pages;
+  a.max_pages = max_pages;
+  a.out = out;
+  a.max_logit = max_logit;
+  a.lse = lse;
+  a.workspace = workspace;
+  a.workspace_bytes = workspace_bytes;
+  a.err = device_error_word();
+  if (a.err == nullptr) return fail(MSA_ERR_CUDA, std::string(fn) + ": no device error word");
+  const char* why = nullptr;
+  cudaError_t e = launch_sparse_attn(a, reinterpret_cast<cudaStream_t>(stream), &why);
+  if (e != cudaSuccess) return cuda_fail(e, fn, why);
+  return MSA_OK;
+}
+
+msa_status msa_sparse_mla_fwd(const uint8_t* q, const uint8_t* kv, const int32_t* indices,
+                              const int32_t* topk_length, const float* sink, float sm_scale,
+                              const float* q_scale, const float* kv_scale, int T, int H, int S_kv,
+                              int d_qk, int d_v, int topk, uint16_t* out, float* max_logits,
+                              float* lse, msa_stream_t stream) {
+  const char* fn = "msa_sparse_mla_fwd";
+  if (d_v != 512) return fail(MSA_ERR_UNSUPPORTED, std::string(fn) + ": d_v must be 512");
+  if (d_qk != 576) return fail(MSA_ERR_UNSUPPORTED, std::string(fn) + ": d_qk must be 576");
+  if (H != 128) return fail(MSA_ERR_UNSUPPORTED, std::string(fn) + ": H must be 128");
+  if (T < 0 || S_kv < 1) return fail(MSA_ERR_INVALID_ARG, std::string(fn) + ": bad T / S_kv");
+  if (topk < 64 || topk % 64 != 0)
+    return fail(MSA_ERR_UNSUPPORTED, std::string(fn) + ": topk must be a positive multiple of 64");
+  if (!std::isfinite(sm_scale) || !(sm_scale > 0.0f))
+    return fail(MSA_ERR_INVALID_ARG, std::string(fn) + ": sm_scale must be finite and > 0");
+  float qs, kvs;
+  if (!read_scale(q_scale, &qs, "q_scale") || !read_scale(kv_scale, &kvs, "kv_scale"))
+    return MSA_ERR_INVALID_ARG;
+  if (T == 0) return MSA_OK;
+  if (!q || !kv || !indices || !out || !max_logits || !lse)
+    return fail(MSA_ERR_INVALID_ARG, std::string(fn) + ": null pointer");
+  if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(out, 16))
+    return fail(MSA_ERR_INVALID_ARG, std::string(fn) + ": q/kv/out must be 16-byte aligned");
+  MlaArgs a{};
+  a.q = q;
+  a.kv = kv;
+  a.indices = indices;
+  a.topk_length = topk_length;
+  a.sink = sink;
+  a.c_sink = sm_scale * qs;
+  a.c_qk = a.c_sink * kvs;
+  a.v_scale = kvs;
+  a.T = T;
+  a.H = H;
+  a.S_kv = S_kv;
+  a.d_qk = d_qk;
+  a.d_v = d_v;
+  a.topk = topk;
+  a.out = out;
+  a.max_logits = max_logits;
+  a.lse = lse;
+  a.err = device_error_word();
+  if (a.err == nullptr) return fail(MSA_ERR_CUDA, std::string(fn) + ": no device error word");
+  const char* why = nullptr;
+  cudaError_t e = launch_sparse_mla(a, reinterpret_cast<cudaStream_t>(stream), &why);
+  if (e != cudaSuccess) return cuda_fail(e, fn, why);
+  return MSA_OK;
+}
+
+}  // extern "C"

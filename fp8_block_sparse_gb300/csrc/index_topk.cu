@@ -1,0 +1,423 @@
+// index_topk.cu -- step (b): indexer block scores and the ascending top-k.
+//
+// What is computed (vLLM PR 45892 page, implementation steps 1-4; sglang PR
+// 30971 page, implementation step 2 and review item 2): for index head i and
+// query token t at position p with own block o = p / 128,
+//   score[i,t,j] = max over the 128 keys of block j < o of idx_q[t,i] . idx_k[key]
+// and topk_indices[i,t,:] lists the topk-1 best blocks j < o (ties: lower id)
+// in ascending order followed by o; when o + 1 <= topk it lists 0..o and pads
+// with -1. The own block is always selected (a reading of this library).
+//
+// GB300 design:
+// * Prefill scoring is a dense FP8 contraction, so it runs on tcgen05: a CTA
+//   holds a 128-row tile of (token, index head) queries in shared memory (one
+//   TMA load) and streams the 128-key pages of the index-K cache through a
+//   4-stage TMA ring. Each page is one M=128 x N=128 x K=D e4m3 MMA into a
+//   double-buffered TMEM accumulator; four epilogue warps read their rows out
+//   of TMEM and reduce the 128 columns to the block maximum. Scores of a
+//   32-block chunk are staged in shared memory and written as contiguous rows.
+// * Decode (one query token per sequence) is a stream over the index-K pages;
+//   it runs the same MMA with the roles swapped (M=128 keys of the page,
+//   N=16 query columns of which Hidx are used) so the page is the A operand
+//   straight out of the TMA ring and the max runs across TMEM lanes.
+// * Selection is one warp per row: a 32-step radix select finds the
+//   (topk-1)-th largest score bit-exactly on the fp32 key, then ballot/popc
+//   writes the chosen ids in ascending order.
+#include "common.cuh"
+#include "internal.h"
+#include "plan.cuh"
+
+namespace msa {
+namespace {
+
+constexpr int kChunk = 32;       // blocks scored per CTA
+constexpr int kStages = 4;       // TMA ring depth
+constexpr int kScorePitch = kChunk + 1;
+
+// Order-preserving map of fp32 onto uint32 (larger float -> larger key).
+MSA_DEV uint32_t order_key(float x) {
+  uint32_t u = __float_as_uint(x);
+  if (u == 0x80000000u) u = 0;                        // -0 ranks as +0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+MSA_DEV float key_to_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// ------------------------------------------------------------ prefill scores
+template <int D>
+struct PrefillSmem {
+  static constexpr int kQ = 0;                               // 128 x D
+  static constexpr int kK = 16384;                           // kStages x (128 x D)
+  static constexpr int kScore = kK + kStages * 16384;        // 128 x kScorePitch fp32
+  static constexpr int kBytes = kScore + 128 * kScorePitch * 4 + 1024;   // + alignment slack
+};
+
+template <int D>
+__global__ void __launch_bounds__(192, 1)
+index_score_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
+                           const __grid_constant__ CUtensorMap tm_k,
+                           const int32_t* __restrict__ page_table,
+                           const TileInfo* __restrict__ tiles, const int* __restrict__ n_tiles_p,
+                           int T, int Hidx, int toks, int max_pages, int num_pages,
+                           int chunks_per_tile, float* __restrict__ scores, unsigned* err) {
+  constexpr int SWZ = D;                    // 128-byte or 64-byte swizzle rows
+  constexpr uint32_t kIdesc = idesc_f32(128, 128);
+  using L = PrefillSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t bar_q, bar_full[kStages], bar_empty[kStages], bar_tfull[2], bar_tempty[2];
+  __shared__ uint32_t tmem_base_s;
+
+  const int n_tiles = *n_tiles_p;
+  const int tile_rank = blockIdx.x / chunks_per_tile;
+  if (tile_rank >= n_tiles) return;
+  const int tile_id = n_tiles - 1 - tile_rank;      // longest (latest) tiles first
+  const TileInfo ti = tiles[tile_id];
+  const int n_tok = min(toks, ti.t_end - ti.t0);
+  const int nb = (ti.p0 + n_tok - 1) / 128;        // blocks 0..nb-1 can be needed
+  const int c0 = (blockIdx.x % chunks_per_tile) * kChunk;
+  if (c0 >= nb) return;
+  const int nblk = min(kChunk, nb - c0);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  uint8_t* sQ = smem + L::kQ;
+  uint8_t* sK = smem + L::kK;
+  float* sScore = reinterpret_cast<float*>(smem + L::kScore);
+
+  if (tid == 0) {
+    mbar_init(&bar_q, 1);
+    for (int s = 0; s < kStages; ++s) { mbar_init(&bar_full[s], 1); mbar_init(&bar_empty[s], 1); }
+    for (int s = 0; s < 2; ++s) { mbar_init(&bar_tfull[s], 1); mbar_init(&bar_tempty[s], 4); }
+    fence_barrier_init();
+  }
+  if (warp == 1) { tmem_alloc(&tmem_base_s, 256); tmem_relinquish(); }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_s;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      mbar_arrive_expect_tx(&bar_q, 128 * D);
+      tma_load_2d(sQ, &tm_q, &bar_q, 0, ti.t0 * Hidx);
+      const int32_t* prow = page_table + size_t(ti.b) * max_pages;
+      for (int j = 0; j < nblk; ++j) {
+        const int s = j % kStages;
+        if (!mbar_wait(&bar_empty[s], ((j / kStages) & 1) ^ 1, err)) break;
+        int page = __ldg(prow + c0 + j);
+        if (page < 0 || page >= num_pages) { atomicOr(err, MSA_DEVERR_DATA); page = 0; }
+        mbar_arrive_expect_tx(&bar_full[s], 128 * D);
+        tma_load_2d(sK + s * 16384, &tm_k, &bar_full[s], 0, page * 128);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && mbar_wait(&bar_q, 0, err)) {
+      for (int j = 0; j < nblk; ++j) {
+        const int s = j % kStages, buf = j & 1;
+        if (!mbar_wait(&bar_full[s], (j / kStages) & 1, err)) break;
+        if (!mbar_wait(&bar_tempty[buf], ((j >> 1) & 1) ^ 1, err)) break;
+        tc_fence_after();
+        const uint32_t aq = smem_addr(sQ), bk = smem_addr(sK + s * 16384);
+#pragma unroll
+        for (int k = 0; k < D / 32; ++k)
+          mma_e4m3(tmem + buf * 128, sdesc_kmajor(aq + 32 * k, SWZ), sdesc_kmajor(bk + 32 * k, SWZ),
+                   kIdesc, k > 0);
+        mma_commit(&bar_empty[s]);
+        mma_commit(&bar_tfull[buf]);
+      }
+    }
+  } else {
+    // epilogue: warps 2..5 own TMEM lanes 32*(warp%4) .. +31
+    const int row = (warp & 3) * 32 + lane;
+    for (int j = 0; j < nblk; ++j) {
+      const int buf = j & 1;
+      if (!mbar_wait(&bar_tfull[buf], (j >> 1) & 1, err)) break;
+      tc_fence_after();
+      float m = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 128; c += 32) {
+        uint32_t v[32];
+        tmem_ld32(tmem_addr(tmem + buf * 128, (warp & 3) * 32, c), v);
+#pragma unroll
+        for (int x = 0; x < 32; ++x) m = fmaxf(m, __uint_as_float(v[x]));
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_tempty[buf]);
+      sScore[row * kScorePitch + j] = m;
+    }
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    // rows -> (token, head); each row writes its nblk scores contiguously
+    const int et = tid - 64;
+    for (int x = et; x < 128 * nblk; x += 128) {
+      const int r = x / nblk, jj = x - r * nblk;
+      const int tok = ti.t0 + r / Hidx, head = r % Hidx;
+      if (r / Hidx < n_tok)
+        scores[(size_t(head) * T + tok) * max_pages + c0 + jj] = sScore[r * kScorePitch + jj];
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, 256);
+}
+
+// ------------------------------------------------------------ decode scores
+// One CTA per (query token, 32-block chunk). A = index-K page (M = 128 keys),
+// B = the token's Hidx query rows (N = 16; extra rows are ignored).
+template <int D>
+__global__ void __launch_bounds__(192, 1)
+index_score_decode_kernel(const __grid_constant__ CUtensorMap tm_q,
+                          const __grid_constant__ CUtensorMap tm_k,
+                          const int32_t* __restrict__ page_table,
+                          const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ cu_q,
+                          int B, int T, int Hidx, int max_pages, int num_pages,
+                          int chunks_per_tok, float* __restrict__ scores, unsigned* err) {
+  constexpr int SWZ = D;
+  constexpr int kBufs = 4;
+  constexpr uint32_t kIdesc = idesc_f32(128, 16);
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t bar_q, bar_full[kStages], bar_empty[kStages], bar_tfull[kBufs], bar_tempty[kBufs];
+  __shared__ uint32_t tmem_base_s;
+  __shared__ uint32_t sred[kChunk][16];   // order-preserving keys of the block maxima
+
+  const int t = blockIdx.x / chunks_per_tok;
+  const int c0 = (blockIdx.x % chunks_per_tok) * kChunk;
+  const int b = find_sequence(cu_q, B, t);
+  const int qlen = cu_q[b + 1] - cu_q[b];
+  const int p = seq_lens[b] - qlen + (t - cu_q[b]);
+  if (p < 0 || p >= max_pages * 128) {
+    if (threadIdx.x == 0 && c0 == 0) atomicOr(err, MSA_DEVERR_DATA);
+    return;
+  }
+  const int nb = p / 128;
+  if (c0 >= nb) return;
+  const int nblk = min(kChunk, nb - c0);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  uint8_t* sK = smem;                       // kStages x 16 KB
+  uint8_t* sQ = smem + kStages * 16384;     // 16 rows x D
+
+  if (tid == 0) {
+    mbar_init(&bar_q, 1);
+    for (int s = 0; s < kStages; ++s) { mbar_init(&bar_full[s], 1); mbar_init(&bar_empty[s], 1); }
+    for (int s = 0; s < kBufs; ++s) { mbar_init(&bar_tfull[s], 1); mbar_init(&bar_tempty[s], 4); }
+    fence_barrier_init();
+  }
+  if (warp == 1) { tmem_alloc(&tmem_base_s, 64); tmem_relinquish(); }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_s;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&bar_q, 16 * D);
+      tma_load_2d(sQ, &tm_q, &bar_q, 0, t * Hidx);
+      const int32_t* prow = page_table + size_t(b) * max_pages;
+      for (int j = 0; j < nblk; ++j) {
+        const int s = j % kStages;
+        if (!mbar_wait(&bar_empty[s], ((j / kStages) & 1) ^ 1, err)) break;
+        int page = __ldg(prow + c0 + j);
+        if (page < 0 || page >= num_pages) { atomicOr(err, MSA_DEVERR_DATA); page = 0; }
+        mbar_arrive_expect_tx(&bar_full[s], 128 * D);
+        tma_load_2d(sK + s * 16384, &tm_k, &bar_full[s], 0, page * 128);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && mbar_wait(&bar_q, 0, err)) {
+      for (int j = 0; j < nblk; ++j) {
+        const int s = j % kStages, buf = j % kBufs;
+        if (!mbar_wait(&bar_full[s], (j / kStages) & 1, err)) break;
+        if (!mbar_wait(&bar_tempty[buf], ((j / kBufs) & 1) ^ 1, err)) break;
+        tc_fence_after();
+        const uint32_t ak = smem_addr(sK + s * 16384), bq = smem_addr(sQ);
+#pragma unroll
+        for (int k = 0; k < D / 32; ++k)
+          mma_e4m3(tmem + buf * 16, sdesc_kmajor(ak + 32 * k, SWZ), sdesc_kmajor(bq + 32 * k, SWZ),
+                   kIdesc, k > 0);
+        mma_commit(&bar_empty[s]);
+        mma_commit(&bar_tfull[buf]);
+      }
+    }
+  } else {
+    const int q4 = warp & 3;
+    const int et = tid - 64;
+    for (int x = et; x < kChunk * 16; x += 128) (&sred[0][0])[x] = 0u;
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    for (int j = 0; j < nblk; ++j) {
+      const int buf = j % kBufs;
+      if (!mbar_wait(&bar_tfull[buf], (j / kBufs) & 1, err)) break;
+      tc_fence_after();
+      uint32_t v[16];
+      tmem_ld16(tmem_addr(tmem + buf * 16, q4 * 32, 0), v);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_tempty[buf]);
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        float m = __uint_as_float(v[c]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0 && c < Hidx) atomicMax(&sred[j][c], order_key(m));
+      }
+    }
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    for (int x = et; x < nblk * Hidx; x += 128) {
+      const int c = x / nblk, j = x - c * nblk;
+      scores[(size_t(c) * T + t) * max_pages + c0 + j] = key_to_float(sred[j][c]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, 64);
+}
+
+// ------------------------------------------------------------ selection
+
+// One warp per (index head, token) row. NPL = candidate slots per lane.
+template <int NPL>
+__global__ void __launch_bounds__(256)
+topk_select_kernel(const float* __restrict__ scores, const int32_t* __restrict__ seq_lens,
+                   const int32_t* __restrict__ cu_q, int B, int T, int Hidx, int topk,
+                   int max_pages, int32_t* __restrict__ out, unsigned* err) {
+  const int lane = threadIdx.x & 31;
+  const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= (long long)Hidx * T) return;
+  const int i = int(row / T), t = int(row % T);
+  const int b = find_sequence(cu_q, B, t);
+  const int qlen = cu_q[b + 1] - cu_q[b];
+  const int p = seq_lens[b] - qlen + (t - cu_q[b]);
+  int32_t* o = out + size_t(row) * topk;
+  if (p < 0 || p >= max_pages * 128) {
+    for (int j = lane; j < topk; j += 32) o[j] = -1;
+    if (lane == 0) atomicOr(err, MSA_DEVERR_DATA);
+    return;
+  }
+  const int own = p / 128;
+  if (own + 1 <= topk) {
+    for (int j = lane; j < topk; j += 32) o[j] = (j <= own) ? j : -1;
+    return;
+  }
+  const int kp = topk - 1;
+  const float* s = scores + (size_t(i) * T + t) * max_pages;
+  uint32_t key[NPL];
+#pragma unroll
+  for (int r = 0; r < NPL; ++r) {
+    const int id = r * 32 + lane;
+    key[r] = id < own ? order_key(__ldg(s + id)) : 0u;   // 0 sorts below every score
+  }
+  // largest tau with #{key >= tau} >= kp: the kp-th largest key
+  uint32_t tau = 0;
+  for (int bit = 31; bit >= 0; --bit) {
+    const uint32_t tr = tau | (1u << bit);
+    int cnt = 0;
+#pragma unroll
+    for (int r = 0; r < NPL; ++r) cnt += key[r] >= tr;
+    cnt = __reduce_add_sync(0xffffffffu, cnt);
+    if (cnt >= kp) tau = tr;
+  }
+  int gt = 0;
+#pragma unroll
+  for (int r = 0; r < NPL; ++r) gt += key[r] > tau;
+  gt = __reduce_add_sync(0xffffffffu, gt);
+  const int need_ties = kp - gt;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  int pos = 0, ties_seen = 0;
+#pragma unroll
+  for (int r = 0; r < NPL; ++r) {
+    const int id = r * 32 + lane;
+    const bool valid = id < own;
+    const bool tie = valid && key[r] == tau;
+    const uint32_t tie_mask = __ballot_sync(0xffffffffu, tie);
+    const int tie_rank = ties_seen + __popc(tie_mask & lt_mask);
+    const bool sel = valid && (key[r] > tau || (tie && tie_rank < need_ties));
+    const uint32_t sel_mask = __ballot_sync(0xffffffffu, sel);
+    if (sel) o[pos + __popc(sel_mask & lt_mask)] = id;
+    pos += __popc(sel_mask);
+    ties_seen += __popc(tie_mask);
+  }
+  if (lane == 0) o[kp] = own;
+}
+
+}  // namespace
+
+size_t index_workspace_bytes(int T, int Hidx, int max_pages) {
+  const size_t scores = align256(size_t(Hidx) * T * max_pages * sizeof(float));
+  const size_t toks = Hidx > 0 ? size_t(128 / Hidx > 0 ? 128 / Hidx : 1) : 1;
+  const size_t max_tiles = (size_t(T) + toks - 1) / toks + size_t(T) + 1;
+  return scores + align256(max_tiles * sizeof(TileInfo)) + 256;
+}
+
+cudaError_t launch_index_topk(const IndexArgs& a, cudaStream_t stream, const char** why) {
+  const int D = a.D;
+  if (a.Hidx > 16 || (a.Hidx & (a.Hidx - 1)) != 0) {
+    *why = "Hidx must be a power of two <= 16";
+    return cudaErrorNotSupported;
+  }
+  if (a.max_pages > 2048) {
+    *why = "max_pages must be <= 2048";
+    return cudaErrorNotSupported;
+  }
+  uint8_t* ws = reinterpret_cast<uint8_t*>(a.scores);
+  float* scores = a.scores;
+  const size_t scores_bytes = align256(size_t(a.Hidx) * a.T * a.max_pages * sizeof(float));
+  const int toks = 128 / a.Hidx;
+  const int max_tiles = (a.T + toks - 1) / toks + a.T + 1;
+  TileInfo* tiles = reinterpret_cast<TileInfo*>(ws + scores_bytes);
+  int* n_tiles = reinterpret_cast<int*>(ws + scores_bytes + align256(size_t(max_tiles) * sizeof(TileInfo)));
+
+  const CUtensorMapSwizzle swz = D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  CUtensorMap tm_q, tm_k;
+  const bool decode = a.max_q_len == 1;
+  {
+    const uint64_t dims[2] = {uint64_t(D), uint64_t(a.T) * a.Hidx};
+    const uint64_t strides[1] = {uint64_t(D)};
+    const uint32_t box[2] = {uint32_t(D), decode ? 16u : 128u};
+    if (!encode_tensor_map(&tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.idx_q, dims, strides, box, swz, why))
+      return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[2] = {uint64_t(D), uint64_t(a.num_pages) * 128};
+    const uint64_t strides[1] = {uint64_t(D)};
+    const uint32_t box[2] = {uint32_t(D), 128u};
+    if (!encode_tensor_map(&tm_k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.idx_k, dims, strides, box, swz, why))
+      return cudaErrorInvalidValue;
+  }
+  const int chunks = (a.max_pages + kChunk - 1) / kChunk;
+  if (decode) {
+    const int smem = kStages * 16384 + 16 * 128 + 1024;
+    auto kern = D == 128 ? index_score_decode_kernel<128> : index_score_decode_kernel<64>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<a.T * chunks, 192, smem, stream>>>(tm_q, tm_k, a.page_table, a.seq_lens, a.cu_q, a.B, a.T,
+                                              a.Hidx, a.max_pages, a.num_pages, chunks, scores, a.err);
+  } else {
+    plan_tiles_kernel<<<1, 256, 0, stream>>>(a.seq_lens, a.cu_q, a.B, toks, a.max_pages, max_tiles,
+                                            tiles, n_tiles, a.err);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int smem = D == 128 ? PrefillSmem<128>::kBytes : PrefillSmem<64>::kBytes;
+    auto kern = D == 128 ? index_score_prefill_kernel<128> : index_score_prefill_kernel<64>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    const int n_tiles_max = (a.T + toks - 1) / toks + a.B;
+    kern<<<n_tiles_max * chunks, 192, smem, stream>>>(tm_q, tm_k, a.page_table, tiles, n_tiles, a.T,
+                                                      a.Hidx, toks, a.max_pages, a.num_pages, chunks,
+                                                      scores, a.err);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long long rows = (long long)a.Hidx * a.T;
+  const int grid = int((rows + 7) / 8);
+  if (a.max_pages <= 256)
+    topk_select_kernel<8><<<grid, 256, 0, stream>>>(scores, a.seq_lens, a.cu_q, a.B, a.T, a.Hidx, a.topk, a.max_pages, a.topk_indices, a.err);
+  else if (a.max_pages <= 512)
+    topk_select_kernel<16><<<grid, 256, 0, stream>>>(scores, a.seq_lens, a.cu_q, a.B, a.T, a.Hidx, a.topk, a.max_pages, a.topk_indices, a.err);
+  else
+    topk_select_kernel<64><<<grid, 256, 0, stream>>>(scores, a.seq_lens, a.cu_q, a.B, a.T, a.Hidx, a.topk, a.max_pages, a.topk_indices, a.err);
+  return cudaGetLastError();
+}
+
+}  // namespace msa

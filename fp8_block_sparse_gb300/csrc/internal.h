@@ -1,0 +1,87 @@
+// internal.h -- launchers shared between the C-ABI layer (api.cu) and the
+// kernel translation units. Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace msa {
+
+// Bits of the device error word.
+constexpr unsigned MSA_DEVERR_DATA = 1u;     // bad page id / index seen by a kernel
+constexpr unsigned MSA_DEVERR_TIMEOUT = 2u;  // a bounded wait gave up
+
+// Device address of this device's error word (set up once per device).
+unsigned* device_error_word();
+
+// Builds a tiled TMA descriptor through the driver entry point. Returns false
+// (and fills `why`) when the driver rejects it.
+bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base,
+                       const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
+                       CUtensorMapSwizzle swizzle, const char** why);
+
+int num_sms();
+
+// Step (a).
+cudaError_t launch_quant(const void* x, bool bf16, int64_t rows, int64_t cols, int64_t x_stride,
+                         uint8_t* out, int64_t out_stride, float s_inv, cudaStream_t stream);
+
+// Step (b). Scores go to `scores` [Hidx][T][max_pages] fp32 (workspace).
+struct IndexArgs {
+  const uint8_t* idx_q;
+  const uint8_t* idx_k;
+  const int32_t* page_table;
+  const int32_t* seq_lens;
+  const int32_t* cu_q;
+  int B, T, max_q_len, Hidx, D, topk, num_pages, max_pages;
+  int32_t* topk_indices;
+  float* scores;
+  int32_t* tile_map;   // workspace: per-CTA (sequence, first token) list for prefill tiles
+  unsigned* err;
+};
+cudaError_t launch_index_topk(const IndexArgs& a, cudaStream_t stream, const char** why);
+size_t index_workspace_bytes(int T, int Hidx, int max_pages);
+
+// Step (c), GQA.
+struct AttnArgs {
+  const uint8_t* q;
+  const uint8_t* k_cache;
+  const uint8_t* v_cache;
+  const int32_t* page_table;
+  const int32_t* seq_lens;
+  const int32_t* cu_q;
+  const int32_t* topk;
+  const float* sink;
+  float c_qk;      // sm_scale * q_scale * k_scale
+  float c_sink;    // sm_scale * q_scale
+  float v_scale;
+  int B, T, max_q_len, Hq, Hkv, Hidx, D, topk_k, num_pages, max_pages;
+  uint16_t* out;
+  float* max_logit;
+  float* lse;
+  void* workspace;
+  size_t workspace_bytes;
+  unsigned* err;
+};
+cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream, const char** why);
+size_t attn_workspace_bytes(int B, int T, int max_q_len, int Hkv, int D, int max_pages);
+
+// Step (c), sparse MLA.
+struct MlaArgs {
+  const uint8_t* q;
+  const uint8_t* kv;
+  const int32_t* indices;
+  const int32_t* topk_length;
+  const float* sink;
+  float c_qk, c_sink, v_scale;
+  int T, H, S_kv, d_qk, d_v, topk;
+  uint16_t* out;
+  float* max_logits;
+  float* lse;
+  unsigned* err;
+};
+cudaError_t launch_sparse_mla(const MlaArgs& a, cudaStream_t stream, const char** why);
+
+}  // namespace msa

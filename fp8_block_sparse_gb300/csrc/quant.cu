@@ -1,0 +1,158 @@
+// quant.cu -- step (a): per-tensor e4m3 quantisation, out = e4m3(fp32(x) * s_inv).
+//
+// sglang PR 25460 page, key source excerpt of fp8_quantize (widen to fp32,
+// multiply by a host-side scale_inv, cast to fp8); sglang PR 30971 page,
+// implementation step 3 (_quant_q_fp8 on q and idx_q).
+//
+// Pure streaming work (2 bytes in, 1 byte out per element), so the kernel is
+// built for HBM: each thread moves 16 elements per step as two 16-byte loads
+// and one 16-byte store, several steps in flight, over a grid sized to the
+// SM count. The multiply is __fmul_rn (never contracted) and the cast is the
+// hardware round-to-nearest-even satfinite conversion.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace msa {
+namespace {
+
+MSA_DEV uint16_t cvt2(float a, float b) {
+  return __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+}
+
+// 8 bf16 / fp16 values packed in a uint4 -> 8 fp32 values.
+template <bool BF16>
+MSA_DEV void widen8(const uint4& u, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (BF16) {
+      f[2 * i] = __uint_as_float(w[i] << 16);
+      f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    } else {
+      __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
+      float2 p = __half22float2(h);
+      f[2 * i] = p.x;
+      f[2 * i + 1] = p.y;
+    }
+  }
+}
+
+template <bool BF16>
+MSA_DEV uint4 quant16(const uint4& lo, const uint4& hi, float s_inv) {
+  float a[8], b[8];
+  widen8<BF16>(lo, a);
+  widen8<BF16>(hi, b);
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    o[i] = uint32_t(cvt2(__fmul_rn(a[4 * i], s_inv), __fmul_rn(a[4 * i + 1], s_inv))) |
+           (uint32_t(cvt2(__fmul_rn(a[4 * i + 2], s_inv), __fmul_rn(a[4 * i + 3], s_inv))) << 16);
+    o[2 + i] = uint32_t(cvt2(__fmul_rn(b[4 * i], s_inv), __fmul_rn(b[4 * i + 1], s_inv))) |
+               (uint32_t(cvt2(__fmul_rn(b[4 * i + 2], s_inv), __fmul_rn(b[4 * i + 3], s_inv))) << 16);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// Rows of `cols` elements (cols % 16 == 0, 16-byte aligned rows): one chunk
+// = 16 consecutive elements of one row. Contiguous tensors pass
+// chunks_per_row = total chunks and rows = 1.
+template <bool BF16>
+__global__ void __launch_bounds__(256) quant_vec_kernel(const uint16_t* __restrict__ x,
+                                                        uint32_t rows, uint32_t chunks_per_row,
+                                                        int64_t x_stride,
+                                                        uint8_t* __restrict__ out,
+                                                        int64_t out_stride, float s_inv) {
+  const uint64_t total = uint64_t(rows) * chunks_per_row;
+  const uint64_t step = uint64_t(gridDim.x) * blockDim.x;
+  uint64_t c = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  // two chunks per iteration keep 64 bytes of loads in flight per thread
+  for (; c + step < total; c += 2 * step) {
+    const uint64_t c1 = c + step;
+    const uint32_t r0 = uint32_t(c / chunks_per_row), r1 = uint32_t(c1 / chunks_per_row);
+    const uint64_t j0 = (c - uint64_t(r0) * chunks_per_row) * 16;
+    const uint64_t j1 = (c1 - uint64_t(r1) * chunks_per_row) * 16;
+    const uint4* s0 = reinterpret_cast<const uint4*>(x + r0 * x_stride + j0);
+    const uint4* s1 = reinterpret_cast<const uint4*>(x + r1 * x_stride + j1);
+    const uint4 a0 = __ldcs(s0), b0 = __ldcs(s0 + 1), a1 = __ldcs(s1), b1 = __ldcs(s1 + 1);
+    *reinterpret_cast<uint4*>(out + r0 * out_stride + j0) = quant16<BF16>(a0, b0, s_inv);
+    *reinterpret_cast<uint4*>(out + r1 * out_stride + j1) = quant16<BF16>(a1, b1, s_inv);
+  }
+  if (c < total) {
+    const uint32_t r0 = uint32_t(c / chunks_per_row);
+    const uint64_t j0 = (c - uint64_t(r0) * chunks_per_row) * 16;
+    const uint4* s0 = reinterpret_cast<const uint4*>(x + r0 * x_stride + j0);
+    *reinterpret_cast<uint4*>(out + r0 * out_stride + j0) =
+        quant16<BF16>(__ldcs(s0), __ldcs(s0 + 1), s_inv);
+  }
+}
+
+// Any shape, stride and alignment: one element per thread step.
+template <bool BF16>
+__global__ void __launch_bounds__(256) quant_scalar_kernel(const uint16_t* __restrict__ x,
+                                                           int64_t rows, int64_t cols,
+                                                           int64_t x_stride,
+                                                           uint8_t* __restrict__ out,
+                                                           int64_t out_stride, float s_inv) {
+  const int64_t total = rows * cols;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t r = i / cols, j = i - r * cols;
+    const uint16_t bits = x[r * x_stride + j];
+    float v;
+    if (BF16) {
+      v = __uint_as_float(uint32_t(bits) << 16);
+    } else {
+      v = __half2float(__ushort_as_half(bits));
+    }
+    const uint16_t p = cvt2(__fmul_rn(v, s_inv), 0.0f);
+    out[r * out_stride + j] = uint8_t(p & 0xFF);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_quant(const void* x, bool bf16, int64_t rows, int64_t cols, int64_t x_stride,
+                         uint8_t* out, int64_t out_stride, float s_inv, cudaStream_t stream) {
+  if (rows == 0 || cols == 0) return cudaSuccess;
+  const uint16_t* xs = static_cast<const uint16_t*>(x);
+  const bool contiguous = (x_stride == cols) && (out_stride == cols);
+  const bool aligned = (reinterpret_cast<uintptr_t>(x) % 16 == 0) &&
+                       (reinterpret_cast<uintptr_t>(out) % 16 == 0);
+  const int sms = num_sms();
+  const int threads = 256;
+  if (aligned && contiguous && (rows * cols) % 16 == 0 && (rows * cols) / 16 < (1ll << 32)) {
+    const uint64_t chunks = uint64_t(rows * cols) / 16;
+    const uint64_t want = (chunks + 2 * threads - 1) / (2 * threads);
+    const int grid = int(want < uint64_t(sms) * 8 ? (want ? want : 1) : uint64_t(sms) * 8);
+    if (bf16)
+      quant_vec_kernel<true><<<grid, threads, 0, stream>>>(xs, 1, uint32_t(chunks), 0, out, 0, s_inv);
+    else
+      quant_vec_kernel<false><<<grid, threads, 0, stream>>>(xs, 1, uint32_t(chunks), 0, out, 0, s_inv);
+  } else if (aligned && cols % 16 == 0 && x_stride % 8 == 0 && out_stride % 16 == 0 &&
+             rows < (1ll << 32) && rows * (cols / 16) < (1ll << 40)) {
+    const uint64_t chunks = uint64_t(rows) * uint64_t(cols / 16);
+    const uint64_t want = (chunks + 2 * threads - 1) / (2 * threads);
+    const int grid = int(want < uint64_t(sms) * 8 ? (want ? want : 1) : uint64_t(sms) * 8);
+    if (bf16)
+      quant_vec_kernel<true><<<grid, threads, 0, stream>>>(xs, uint32_t(rows), uint32_t(cols / 16),
+                                                           x_stride, out, out_stride, s_inv);
+    else
+      quant_vec_kernel<false><<<grid, threads, 0, stream>>>(xs, uint32_t(rows), uint32_t(cols / 16),
+                                                            x_stride, out, out_stride, s_inv);
+  } else {
+    const int64_t total = rows * cols;
+    const int64_t want = (total + threads - 1) / threads;
+    const int grid = int(want < int64_t(sms) * 8 ? want : int64_t(sms) * 8);
+    if (bf16)
+      quant_scalar_kernel<true><<<grid, threads, 0, stream>>>(xs, rows, cols, x_stride, out, out_stride, s_inv);
+    else
+      quant_scalar_kernel<false><<<grid, threads, 0, stream>>>(xs, rows, cols, x_stride, out, out_stride, s_inv);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace msa

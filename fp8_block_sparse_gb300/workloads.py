@@ -255,3 +255,27 @@ def make_mla(cfg: MLAConfig, seed: Optional[int] = None, T_override: Optional[in
     sink = _rng(seed, _SINK).standard_normal(cfg.H).astype(np.float32)
     scales = {"q": amax_scale(q), "kv": amax_scale(kv)}
     return MLAWorkload(cfg, q, kv, indices, lengths, sink, scales, 1.0 / math.sqrt(cfg.d_qk))
+
+
+def random_topk(seed: int, seq_lens: np.ndarray, cu_q: np.ndarray, Hidx: int, topk: int) -> np.ndarray:
+    """A seeded, valid block selection [Hidx, T, topk] (int32) to drive the
+    attention step on its own: for each row, the query's own block plus
+    topk-1 distinct earlier blocks drawn uniformly, sorted ascending, -1
+    padded when the causal blocks do not exceed topk."""
+    g = _rng(seed, 200)
+    seq_lens = np.asarray(seq_lens, np.int64)
+    cu_q = np.asarray(cu_q, np.int64)
+    T = int(cu_q[-1])
+    out = np.full((Hidx, T, topk), -1, dtype=np.int32)
+    for b in range(len(seq_lens)):
+        q0, q1 = int(cu_q[b]), int(cu_q[b + 1])
+        for t in range(q0, q1):
+            own = (int(seq_lens[b]) - (q1 - q0) + (t - q0)) // PAGE
+            for i in range(Hidx):
+                if own + 1 <= topk:
+                    out[i, t, :own + 1] = np.arange(own + 1)
+                else:
+                    pick = np.sort(g.choice(own, size=topk - 1, replace=False))
+                    out[i, t, :topk - 1] = pick
+                    out[i, t, topk - 1] = own
+    return out

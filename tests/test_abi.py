@@ -1,0 +1,100 @@
+"""Host-side checks of libmsa.so that need no GPU: every symbol include/msa.h
+declares is exported, and argument validation rejects bad calls before any
+CUDA work (these calls return before touching the device)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from fp8_block_sparse_gb300 import build as b
+    b.build()
+    from fp8_block_sparse_gb300 import binding
+    return binding.load()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "msa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(msa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_four_path_entry_points():
+    names = declared_symbols()
+    for n in ("msa_quant_fp8", "msa_index_topk", "msa_sparse_attn_fwd", "msa_sparse_mla_fwd"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", lib._name], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (msa_\w+)", out))
+    missing = [n for n in declared_symbols() if n not in exported]
+    assert not missing, missing
+    for n in declared_symbols():
+        getattr(lib, n)
+
+
+def test_version_and_error_string(lib):
+    assert lib.msa_version() >= 100
+    assert isinstance(lib.msa_last_error_string(), bytes)
+
+
+def _f(x):
+    return ctypes.pointer(ctypes.c_float(x))
+
+
+def test_quant_rejects_e5m2_and_bad_arguments(lib):
+    dummy = ctypes.c_void_p(16)
+    # e5m2 output never enters the path
+    assert lib.msa_quant_fp8(dummy, 0, 4, 16, 16, dummy, 3, 16, None, None) == 2
+    assert b"e5m2" in lib.msa_last_error_string()
+    assert lib.msa_quant_fp8(dummy, 2, 4, 16, 16, dummy, 2, 16, None, None) == 1    # e4m3 input
+    assert lib.msa_quant_fp8(dummy, 0, -1, 16, 16, dummy, 2, 16, None, None) == 1   # negative rows
+    assert lib.msa_quant_fp8(dummy, 0, 4, 16, 8, dummy, 2, 16, None, None) == 1     # stride < cols
+    assert lib.msa_quant_fp8(None, 0, 4, 16, 16, dummy, 2, 16, None, None) == 1     # null x
+    assert lib.msa_quant_fp8(dummy, 0, 4, 16, 16, dummy, 2, 16, _f(0.0), None) == 1  # zero scale
+    assert lib.msa_quant_fp8(dummy, 0, 4, 16, 16, dummy, 2, 16, _f(float("nan")), None) == 1
+    assert lib.msa_quant_fp8(None, 0, 0, 16, 16, None, 2, 16, None, None) == 0      # empty: no-op
+
+
+def test_index_topk_validation(lib):
+    p = ctypes.c_void_p(256)
+    # D unsupported, topk out of range, max_q_len out of range
+    assert lib.msa_index_topk(p, p, p, p, p, 1, 128, 128, 1, 96, 8, 1, 1, p, p, 1 << 20, None) == 2
+    assert lib.msa_index_topk(p, p, p, p, p, 1, 128, 128, 1, 64, 65, 1, 1, p, p, 1 << 20, None) == 2
+    assert lib.msa_index_topk(p, p, p, p, p, 1, 128, 129, 1, 64, 8, 1, 1, p, p, 1 << 20, None) == 1
+    assert lib.msa_index_topk(p, p, p, p, p, 1, 0, 1, 1, 64, 8, 1, 1, p, p, 0, None) == 0   # T = 0
+    need = lib.msa_index_topk_workspace_size(4096, 4, 32)
+    if need:
+        assert lib.msa_index_topk(p, p, p, p, p, 1, 4096, 4096, 4, 64, 8, 32, 32, p, p, need - 1, None) == 5
+
+
+def test_attention_validation(lib):
+    p = ctypes.c_void_p(256)
+    args = lambda hq, hkv, hidx, d, topk, sm=0.1: (p, p, p, p, p, p, p, None, sm, None, None, None,
+                                                    1, 256, 256, hq, hkv, hidx, d, topk, 2, 2,
+                                                    p, p, p, p, 1 << 30, None)
+    assert lib.msa_sparse_attn_fwd(*args(16, 2, 4, 64, 16)) == 2       # head_dim 64
+    assert lib.msa_sparse_attn_fwd(*args(16, 3, 4, 128, 16)) == 1      # Hq % Hkv
+    assert lib.msa_sparse_attn_fwd(*args(12, 1, 4, 128, 16)) == 2      # group 12 not a power of 2
+    assert lib.msa_sparse_attn_fwd(*args(16, 2, 4, 128, 65)) == 2      # topk > 64
+    assert lib.msa_sparse_attn_fwd(*args(16, 2, 4, 128, 16, -1.0)) == 1
+    a = list(args(16, 2, 4, 128, 16))
+    a[10] = _f(-2.0)                                                   # negative k_scale
+    assert lib.msa_sparse_attn_fwd(*a) == 1
+
+
+def test_mla_validation(lib):
+    p = ctypes.c_void_p(256)
+    f = lambda dqk, dv, h, topk: lib.msa_sparse_mla_fwd(p, p, p, None, None, 0.04, None, None,
+                                                         16, h, 1024, dqk, dv, topk, p, p, p, None)
+    assert f(576, 256, 128, 2048) == 2          # d_v must be 512
+    assert f(512, 512, 128, 2048) == 2          # d_qk must be 576
+    assert f(576, 512, 64, 2048) == 2           # 128 heads

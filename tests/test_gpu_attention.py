@@ -1,0 +1,110 @@
+"""GPU parity of msa_sparse_attn_fwd (steps a4/a5) against the oracle.
+
+Bar (stated for this path): O within max-abs 4e-2 and relative Frobenius
+1e-2 of the float64 oracle, lse within 2e-3 absolute; max_logit is an fp32
+dot times the folded scale and is held to 1e-4 relative.
+"""
+
+import numpy as np
+import pytest
+
+from fp8_block_sparse_gb300 import workloads as wl
+from oracle import quant as oq, attention as oa
+from gpu_helpers import dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _codes(w):
+    return (oq.quantize(w.q, w.scales["q"]), oq.quantize(w.k_pool, w.scales["k"]),
+            oq.quantize(w.v_pool, w.scales["v"]))
+
+
+def _check(got, ref, tol_abs=4e-2, tol_rel=1e-2, tol_lse=2e-3):
+    o, ml, lse = got
+    o_ref, ml_ref, lse_ref = ref
+    err = np.abs(o - o_ref).max()
+    rel = np.linalg.norm(o - o_ref) / max(np.linalg.norm(o_ref), 1e-30)
+    assert err <= tol_abs and rel <= tol_rel, (err, rel)
+    assert np.abs(lse - lse_ref).max() <= tol_lse
+    fin = np.isfinite(ml_ref)
+    assert np.array_equal(fin, np.isfinite(ml))
+    np.testing.assert_allclose(ml[fin], ml_ref[fin], rtol=1e-4, atol=1e-5)
+    return err, rel
+
+
+def run_attention(msa, w, ids, tokens=None, sink=True, scales=True):
+    q8, k8, v8 = _codes(w)
+    sc = w.scales if scales else {"q": None, "k": None, "v": None}
+    s = w.sink if sink else None
+    o, ml, lse = msa.sparse_attn_fwd(dev(q8), dev(k8), dev(v8), dev(w.page_table), dev(w.seq_lens),
+                                     dev(w.cu_q), dev(ids), None if s is None else dev(s), w.sm_scale,
+                                     sc["q"], sc["k"], sc["v"], w.max_q_len)
+    msa.check_errors()
+    tok = np.arange(w.T) if tokens is None else np.asarray(tokens)
+    got = (o.float().cpu().numpy()[tok].astype(np.float64), ml.cpu().numpy()[tok],
+           lse.cpu().numpy()[tok])
+    ref = oa.sparse_attention(q8, k8, v8, w.page_table, w.seq_lens, w.cu_q, ids, s, w.sm_scale,
+                              sc["q"], sc["k"], sc["v"], tokens=tok)
+    return _check(got, ref)
+
+
+def test_tiny_all_rows(msa):
+    w = wl.make_gqa(wl.CONFIGS["tiny"])
+    ids = wl.random_topk(0, w.seq_lens, w.cu_q, w.cfg.Hidx, w.cfg.topk)
+    run_attention(msa, w, ids)
+
+
+@pytest.mark.parametrize("T", [1, 17, 129, 1000])
+def test_ragged(msa, T):
+    w = wl.make_gqa(wl.CONFIGS["tiny"], T_override=T)
+    ids = wl.random_topk(T, w.seq_lens, w.cu_q, w.cfg.Hidx, w.cfg.topk)
+    run_attention(msa, w, ids)
+
+
+@pytest.mark.parametrize("topk", [1, 2, 5])
+def test_topk_sizes(msa, topk):
+    w = wl.make_gqa(wl.CONFIGS["prefill8k"], T_override=1500)
+    ids = wl.random_topk(topk, w.seq_lens, w.cu_q, w.cfg.Hidx, topk)
+    run_attention(msa, w, ids)
+
+
+@pytest.mark.parametrize("hq,hkv,hidx", [(16, 1, 4), (2, 2, 1), (8, 2, 8), (4, 1, 2)])
+def test_head_layouts(msa, hq, hkv, hidx):
+    cfg = wl.GQAConfig("heads", 1, (700,), 0, hq, hkv, hidx, 128, 64, 3, "channel", seed=hq + hkv)
+    w = wl.make_gqa(cfg)
+    ids = wl.random_topk(5, w.seq_lens, w.cu_q, hidx, 3)
+    run_attention(msa, w, ids)
+
+
+def test_no_sink_and_unit_scales(msa):
+    w = wl.make_gqa(wl.CONFIGS["tiny"], T_override=600)
+    ids = wl.random_topk(3, w.seq_lens, w.cu_q, 1, 8)
+    run_attention(msa, w, ids, sink=False)
+    run_attention(msa, w, ids, scales=False)
+
+
+def test_varlen_prefill_with_prefix(msa):
+    cfg = wl.GQAConfig("varlen", 3, (700, 1500, 2100), 0, 16, 2, 4, 128, 128, 8, "channel",
+                       pool_factor=1.2, seed=11)
+    w = wl.make_gqa(cfg)
+    q_lens = np.array([700, 300, 257], np.int32)
+    w.cu_q = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    T = int(w.cu_q[-1])
+    w.q, w.idx_q = w.q[:T], w.idx_q[:T]
+    ids = wl.random_topk(9, w.seq_lens, w.cu_q, 4, 8)
+    run_attention(msa, w, ids)
+
+
+def test_prefill8k_sampled(msa):
+    w = wl.make_gqa(wl.CONFIGS["prefill8k"])
+    ids = wl.random_topk(1, w.seq_lens, w.cu_q, 4, 16)
+    tok = np.sort(np.random.default_rng(0).choice(w.T, size=200, replace=False))
+    run_attention(msa, w, ids, tokens=tok)
+
+
+def test_prefill32k_sampled(msa):
+    w = wl.make_gqa(wl.CONFIGS["prefill32k"])
+    ids = wl.random_topk(2, w.seq_lens, w.cu_q, 4, 64)
+    tok = np.sort(np.random.default_rng(1).choice(w.T, size=48, replace=False))
+    run_attention(msa, w, np.ascontiguousarray(ids), tokens=np.concatenate([tok, [w.T - 1]]))
