@@ -46,7 +46,7 @@ _SIGNATURES = {
     "msa_quant_fp8": ([_P, _I, _I64, _I64, _I64, _P, _I, _I64, _FP, _P], _I),
     "msa_index_topk_workspace_size": ([_I, _I, _I], _SZ),
     "msa_index_topk": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P], _I),
-    "msa_sparse_attn_workspace_size": ([_I, _I, _I, _I, _I, _I], _SZ),
+    "msa_sparse_attn_workspace_size": ([_I, _I, _I, _I, _I, _I, _I, _I], _SZ),
     "msa_sparse_attn_fwd": ([_P, _P, _P, _P, _P, _P, _P, _P, _F, _FP, _FP, _FP,
                              _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _SZ, _P], _I),
     "msa_sparse_mla_fwd": ([_P, _P, _P, _P, _P, _F, _FP, _FP, _I, _I, _I, _I, _I, _I,
@@ -152,8 +152,9 @@ def index_topk(idx_q: torch.Tensor, idx_k_cache: torch.Tensor, page_table: torch
     return out
 
 
-def sparse_attn_workspace_size(B: int, T: int, max_q_len: int, Hkv: int, D: int, max_pages: int) -> int:
-    return int(load().msa_sparse_attn_workspace_size(B, T, max_q_len, Hkv, D, max_pages))
+def sparse_attn_workspace_size(B: int, T: int, max_q_len: int, Hq: int, Hkv: int, Hidx: int,
+                               topk: int, max_pages: int) -> int:
+    return int(load().msa_sparse_attn_workspace_size(B, T, max_q_len, Hq, Hkv, Hidx, topk, max_pages))
 
 
 def sparse_attn_fwd(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
@@ -179,7 +180,7 @@ def sparse_attn_fwd(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tenso
     out = torch.empty((T, Hq, D), dtype=torch.bfloat16, device=dev) if out is None else out
     max_logit = torch.empty((T, Hq), dtype=torch.float32, device=dev) if max_logit is None else max_logit
     lse = torch.empty((T, Hq), dtype=torch.float32, device=dev) if lse is None else lse
-    ws_bytes = sparse_attn_workspace_size(B, T, max_q_len, Hkv, D, max_pages)
+    ws_bytes = sparse_attn_workspace_size(B, T, max_q_len, Hq, Hkv, Hidx, topk, max_pages)
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
     _check(lib.msa_sparse_attn_fwd(

@@ -225,9 +225,12 @@ msa_status msa_index_topk(const uint8_t* idx_q, const uint8_t* idx_k_cache,
   return MSA_OK;
 }
 
-size_t msa_sparse_attn_workspace_size(int B, int T, int max_q_len, int Hkv, int D, int max_pages) {
-  if (B < 0 || T < 0 || max_q_len < 0 || Hkv < 0 || D < 0 || max_pages < 0) return 0;
-  return attn_workspace_bytes(B, T, max_q_len, Hkv, D, max_pages);
+size_t msa_sparse_attn_workspace_size(int B, int T, int max_q_len, int Hq, int Hkv, int Hidx,
+                                      int topk, int max_pages) {
+  if (B < 0 || T < 0 || max_q_len < 0 || Hq < 1 || Hkv < 1 || Hidx < 1 || topk < 0 ||
+      max_pages < 0 || Hq % Hkv != 0 || Hq % Hidx != 0)
+    return 0;
+  return attn_workspace_bytes(B, T, max_q_len, Hq, Hkv, Hidx, topk, max_pages);
 }
 
 msa_status msa_sparse_attn_fwd(const uint8_t* q, const uint8_t* k_cache, const uint8_t* v_cache,
@@ -262,7 +265,7 @@ msa_status msa_sparse_attn_fwd(const uint8_t* q, const uint8_t* k_cache, const u
     return fail(MSA_ERR_INVALID_ARG, std::string(fn) + ": null pointer");
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16))
     return fail(MSA_ERR_INVALID_ARG, std::string(fn) + ": q/k/v/out must be 16-byte aligned");
-  const size_t need = attn_workspace_bytes(B, T, max_q_len, Hkv, D, max_pages);
+  const size_t need = attn_workspace_bytes(B, T, max_q_len, Hq, Hkv, Hidx, topk, max_pages);
   if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256)))
     return fail(MSA_ERR_WORKSPACE, std::string(fn) + ": workspace missing, too small or not 256-byte aligned (need " +
                                        std::to_string(need) + " bytes)");

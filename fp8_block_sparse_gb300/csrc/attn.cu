@@ -103,9 +103,10 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   __shared__ uint64_t bar_q, bar_kf[2], bar_ke[2], bar_vf[2], bar_ve[2], bar_sf[2], bar_se[2],
-      bar_pf[2], bar_pe[2], bar_pv;
+      bar_pf[2], bar_pe[2], bar_pv, bar_done;
   __shared__ uint32_t tmem_base_s;
   __shared__ int n_union_s;
+  __shared__ int abort_s;
 
   const int n_tiles = *n_tiles_p;
   const int tile_rank = blockIdx.x / Hkv;
@@ -122,6 +123,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 
   if (tid < 64) sBits[tid] = 0u;
   if (tid == 0) {
+    abort_s = 0;
     mbar_init(&bar_q, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bar_kf[s], 1); mbar_init(&bar_ke[s], 1);
@@ -130,6 +132,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       mbar_init(&bar_pf[s], 4); mbar_init(&bar_pe[s], 1);
     }
     mbar_init(&bar_pv, 1);
+    mbar_init(&bar_done, 1);
     fence_barrier_init();
   }
   if (warp == 1) { tmem_alloc(&tmem_base_s, 512); tmem_relinquish(); }
@@ -202,10 +205,10 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         const int blk = sBlist[j];
         int page = __ldg(prow + blk);
         if (page < 0 || page >= num_pages) { atomicOr(err, MSA_DEVERR_DATA); page = 0; }
-        if (!mbar_wait(&bar_ke[s], ph, err)) break;
+        if (!mbar_wait_ab(&bar_ke[s], ph, err, &abort_s)) break;
         mbar_arrive_expect_tx(&bar_kf[s], 16384);
         tma_load_2d(smem + kKOff + s * 16384, &tm_k, &bar_kf[s], 0, (page * Hkv + g) * 128);
-        if (!mbar_wait(&bar_ve[s], ph, err)) break;
+        if (!mbar_wait_ab(&bar_ve[s], ph, err, &abort_s)) break;
         mbar_arrive_expect_tx(&bar_vf[s], 32768);
         bulk_load(smem + kVOff + s * 32768,
                   vt_img + ((size_t(ti.b) * max_pages + blk) * Hkv + g) * 32768, 32768, &bar_vf[s]);
@@ -213,13 +216,13 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     }
   } else if (warp == 1) {
     // ---------------- MMA issue: S_{j+1} is issued before PV_j
-    if (lane == 0 && nU > 0 && mbar_wait(&bar_q, 0, err)) {
+    if (lane == 0 && nU > 0 && mbar_wait_ab(&bar_q, 0, err, &abort_s)) {
       const uint32_t sq = smem_addr(smem + kQOff);
       auto issue_s = [&](int j) -> bool {
         const int s = j & 1;
         const uint32_t ph = (j >> 1) & 1;
-        if (!mbar_wait(&bar_kf[s], ph, err)) return false;
-        if (!mbar_wait(&bar_se[s], ph ^ 1, err)) return false;
+        if (!mbar_wait_ab(&bar_kf[s], ph, err, &abort_s)) return false;
+        if (!mbar_wait_ab(&bar_se[s], ph ^ 1, err, &abort_s)) return false;
         tc_fence_after();
         const uint32_t sk = smem_addr(smem + kKOff + s * 16384);
 #pragma unroll
@@ -235,7 +238,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         if (j + 1 < nU && !(ok = issue_s(j + 1))) break;
         const int s = j & 1;
         const uint32_t ph = (j >> 1) & 1;
-        if (!mbar_wait(&bar_pf[s], ph, err) || !mbar_wait(&bar_vf[s], ph, err)) break;
+        if (!mbar_wait_ab(&bar_pf[s], ph, err, &abort_s) || !mbar_wait_ab(&bar_vf[s], ph, err, &abort_s)) break;
         tc_fence_after();
         const uint32_t sp = smem_addr(smem + kPOff + s * 32768);
         const uint32_t sv = smem_addr(smem + kVOff + s * 32768);
@@ -248,6 +251,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         mma_commit(&bar_ve[s]);
         mma_commit(&bar_pe[s]);
         mma_commit(&bar_pv);
+        if (j == nU - 1) mma_commit(&bar_done);
       }
     }
   } else {
@@ -263,7 +267,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       const bool sel = ptr < n_ids && sIds[row * kMaxIds + ptr] == blk;
       ptr += sel ? 1 : 0;
       const int ncol = !sel ? 0 : (blk < own ? 128 : pos - blk * 128 + 1);
-      if (!mbar_wait(&bar_sf[s], ph, err)) break;
+      if (!mbar_wait_ab(&bar_sf[s], ph, err, &abort_s)) break;
       tc_fence_after();
       float x[128];
 #pragma unroll
@@ -284,11 +288,14 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         mx = fmaxf(mx, x[c]);
       }
       m_true = fmaxf(m_true, mx);
+      // P buffer s is free once PV_{j-2} is done; waiting here first also makes
+      // the pv-barrier parity below unambiguous (at most one PV outstanding)
+      if (!mbar_wait_ab(&bar_pe[s], ph ^ 1, err, &abort_s)) break;
       const bool grow = mx > m + kRescale;                    // also when m == -inf
       const bool need_rescale = grow && (m > -INFINITY);
       if (__any_sync(0xffffffffu, need_rescale)) {
         // O holds PV_0..PV_{j-1}: wait for the last one, then scale this warp's rows
-        if (!mbar_wait(&bar_pv, (j - 1) & 1, err)) break;
+        if (!mbar_wait_ab(&bar_pv, (j - 1) & 1, err, &abort_s)) break;
         tc_fence_after();
         const float alpha = need_rescale ? exp2f(m - mx) : 1.0f;
 #pragma unroll
@@ -304,8 +311,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       }
       if (grow) m = mx;
 
-      // P row (f16) into the swizzled A operand of buffer s, once PV_{j-2} is done
-      if (!mbar_wait(&bar_pe[s], ph ^ 1, err)) break;
+      // P row (f16) into the swizzled A operand of buffer s
       const float mref = (m == -INFINITY) ? 0.f : m;
       uint8_t* pbuf = p_row_base + s * 32768;
       float sum = 0.f;
@@ -329,7 +335,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     }
 
     // ---------------- epilogue: O / (l + sink), lse, max_logit
-    if (nU > 0) mbar_wait(&bar_pv, (nU - 1) & 1, err);
+    if (nU > 0) mbar_wait_ab(&bar_done, 0, err, &abort_s);
     tc_fence_after();
     const float sig2 = (sink != nullptr && row_valid) ? sink_scale2 * __ldg(sink + h) : -INFINITY;
     const float M = fmaxf(m, sig2);
@@ -369,11 +375,427 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
+
+// ------------------------------------------------------------ paged decode
+// One CTA per (query token, kv head, chunk): the G q heads of the kv head
+// share one walk over the ascending union of their index heads' selections;
+// the union is cut into at most kDecMaxChunks balanced chunks (flash-decoding
+// split) so that enough CTAs stream pages at once. Per block:
+//   S^T = K Q^T   tcgen05 e4m3, M = 128 keys (the page straight from TMA),
+//                 N = 16 query columns (G used), K = 128;
+//   P             softmax across TMEM lanes: one thread per key, the row max
+//                 of a block combined over the four softmax warps through
+//                 shared memory (one named barrier per block); every thread
+//                 keeps identical copies of the running max of each row and
+//                 its own partial row sums (summed once at the end);
+//   O^T += V^T P^T  tcgen05 f16, A = the page's V^T f16 image written by four
+//                 converter warps, B = P (16 rows x 128 keys, f16).
+// A chunk leaves its unnormalised O, running max, row sum and true max in the
+// workspace; decode_combine_kernel merges the chunks and applies the sink.
+constexpr int kDecChunk = 32;
+constexpr int kDecStages = 3;
+constexpr int kDecMaxList = 1024;   // union entries kept (<= 16 index heads x 64)
+constexpr int kDKOff = 0;            // kDecStages x 16 KB K pages
+constexpr int kDVOff = 49152;        // kDecStages x 16 KB V pages (row-major, unswizzled)
+constexpr int kDVTOff = 98304;       // 2 x 32 KB V^T f16 images
+constexpr int kDPOff = 163840;       // 2 x 4 KB P (16 rows x 128 keys f16)
+constexpr int kDQOff = 172032;       // 16 rows x 128 e4m3
+constexpr int kDListOff = 174080;    // union list (int16)
+constexpr int kDMaskOff = 176128;    // per-entry row mask (uint16)
+constexpr int kDBitsOff = 178176;    // 16 bitmaps x 2048 bits
+constexpr int kDecodeSmem = 178176 + 16 * 256 + 1024;
+constexpr uint32_t kIdescDec = idesc_f32(128, 16);
+
+struct DecodePartial {   // per (token, kv head, chunk, row)
+  float m, l, m_true, pad;
+};
+
+__host__ __device__ inline int dec_max_chunks(int n_idx_per_group, int topk, int max_pages) {
+  const int cap = min(max_pages, n_idx_per_group * topk);
+  return max(1, (cap + kDecChunk - 1) / kDecChunk);
+}
+
+__global__ void __launch_bounds__(320, 1)
+attn_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const int32_t* __restrict__ page_table,
+                   const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ cu_q,
+                   const int32_t* __restrict__ topk, float qk_scale2, int B, int T, int Hq,
+                   int Hkv, int Hidx, int topk_k, int max_pages, int num_pages, int max_chunks,
+                   float* __restrict__ part_o, DecodePartial* __restrict__ part_s,
+                   int* __restrict__ n_chunks_out, unsigned* err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  __shared__ uint64_t bar_q, bar_kvf[kDecStages], bar_kve[kDecStages], bar_sf[2], bar_se[2],
+      bar_pf[2], bar_pe[2], bar_vtf[2], bar_vte[2], bar_pv, bar_done;
+  __shared__ uint32_t tmem_base_s;
+  __shared__ int n_union_s;
+  __shared__ float red[2][4][16];
+  __shared__ float lsum[4][16];
+  __shared__ int abort_s;
+
+  const int G = Hq / Hkv;
+  const int c = blockIdx.x % max_chunks;
+  const int g = (blockIdx.x / max_chunks) % Hkv;
+  const int t = blockIdx.x / (max_chunks * Hkv);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = find_sequence(cu_q, B, t);
+  const int qlen = cu_q[b + 1] - cu_q[b];
+  const int L = seq_lens[b];
+  const int pos = L - qlen + (t - cu_q[b]);
+  const size_t unit = size_t(t) * Hkv + g;
+  if (pos < 0 || pos >= max_pages * 128 || L > max_pages * 128) {
+    if (tid == 0 && c == 0) { atomicOr(err, MSA_DEVERR_DATA); n_chunks_out[unit] = 0; }
+    return;
+  }
+  const int own = pos >> 7;
+  const int hpi = Hq / Hidx;                       // q heads per index head
+  const int i_first = (g * G) / hpi;
+  const int n_idx = (g * G + G - 1) / hpi - i_first + 1;
+
+  int16_t* sList = reinterpret_cast<int16_t*>(smem + kDListOff);
+  uint16_t* sMask = reinterpret_cast<uint16_t*>(smem + kDMaskOff);
+  uint32_t* sBits = reinterpret_cast<uint32_t*>(smem + kDBitsOff);
+  for (int x = tid; x < n_idx * 64; x += 320) sBits[x] = 0u;
+  __syncthreads();
+  for (int x = tid; x < n_idx * topk_k; x += 320) {
+    const int il = x / topk_k;
+    const int id = __ldg(topk + (size_t(i_first + il) * T + t) * topk_k + (x - il * topk_k));
+    if (id < 0) continue;
+    if (id > own) { atomicOr(err, MSA_DEVERR_DATA); continue; }
+    atomicOr(&sBits[il * 64 + (id >> 5)], 1u << (id & 31));
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int base = 0;
+    for (int w0 = 0; w0 < 64; w0 += 32) {
+      uint32_t bits = 0;
+      for (int il = 0; il < n_idx; ++il) bits |= sBits[il * 64 + w0 + lane];
+      const int cnt = __popc(bits);
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      int off = base + incl - cnt;
+      uint32_t bb = bits;
+      while (bb) {
+        const int k = __ffs(bb) - 1;
+        bb &= bb - 1;
+        const int blk = (w0 + lane) * 32 + k;
+        if (off < kDecMaxList) {
+          uint32_t m = 0;
+          for (int r = 0; r < G; ++r) {
+            const int il = (g * G + r) / hpi - i_first;
+            m |= ((sBits[il * 64 + (blk >> 5)] >> (blk & 31)) & 1u) << r;
+          }
+          sList[off] = int16_t(blk);
+          sMask[off] = uint16_t(m);
+        }
+        ++off;
+      }
+      base += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) n_union_s = min(base, kDecMaxList);
+  }
+  __syncthreads();
+  const int nU = n_union_s;
+  const int nch = min(max_chunks, (nU + kDecChunk - 1) / kDecChunk);
+  if (c == 0 && tid == 0) n_chunks_out[unit] = nch;
+  if (c >= nch) return;
+  const int cs = (nU + nch - 1) / nch;
+  const int j0 = c * cs, n = min(nU, j0 + cs) - j0;
+
+  if (tid == 0) {
+    abort_s = 0;
+    mbar_init(&bar_q, 1);
+    for (int s = 0; s < kDecStages; ++s) { mbar_init(&bar_kvf[s], 1); mbar_init(&bar_kve[s], 5); }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bar_sf[s], 1); mbar_init(&bar_se[s], 4);
+      mbar_init(&bar_pf[s], 4); mbar_init(&bar_pe[s], 1);
+      mbar_init(&bar_vtf[s], 4); mbar_init(&bar_vte[s], 1);
+    }
+    mbar_init(&bar_pv, 1);
+    mbar_init(&bar_done, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) { tmem_alloc(&tmem_base_s, 64); tmem_relinquish(); }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_s;          // S^T buffers at cols 0, 16; O^T at 32
+
+  if (warp == 0) {
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&bar_q, 16 * 128);
+      tma_load_2d(smem + kDQOff, &tm_q, &bar_q, 0, t * Hq + g * G);
+      const int32_t* prow = page_table + size_t(b) * max_pages;
+      for (int jj = 0; jj < n; ++jj) {
+        const int s = jj % kDecStages;
+        if (!mbar_wait_ab(&bar_kve[s], ((jj / kDecStages) & 1) ^ 1, err, &abort_s)) break;
+        int page = __ldg(prow + sList[j0 + jj]);
+        if (page < 0 || page >= num_pages) { atomicOr(err, MSA_DEVERR_DATA); page = 0; }
+        const int row0 = (page * Hkv + g) * 128;
+        mbar_arrive_expect_tx(&bar_kvf[s], 32768);
+        tma_load_2d(smem + kDKOff + s * 16384, &tm_k, &bar_kvf[s], 0, row0);
+        tma_load_2d(smem + kDVOff + s * 16384, &tm_v, &bar_kvf[s], 0, row0);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && mbar_wait_ab(&bar_q, 0, err, &abort_s)) {
+      const uint32_t sq = smem_addr(smem + kDQOff);
+      auto issue_s = [&](int jj) -> bool {
+        const int s = jj % kDecStages, sb = jj & 1;
+        if (!mbar_wait_ab(&bar_kvf[s], (jj / kDecStages) & 1, err, &abort_s)) return false;
+        if (!mbar_wait_ab(&bar_se[sb], ((jj >> 1) & 1) ^ 1, err, &abort_s)) return false;
+        tc_fence_after();
+        const uint32_t sk = smem_addr(smem + kDKOff + s * 16384);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_e4m3(tmem + sb * 16, sdesc_kmajor(sk + 32 * k, 128), sdesc_kmajor(sq + 32 * k, 128),
+                   kIdescDec, k > 0);
+        mma_commit(&bar_kve[s]);
+        mma_commit(&bar_sf[sb]);
+        return true;
+      };
+      bool ok = n > 0 && issue_s(0);
+      for (int jj = 0; ok && jj < n; ++jj) {
+        if (jj + 1 < n && !(ok = issue_s(jj + 1))) break;
+        const int sb = jj & 1;
+        const uint32_t ph = (jj >> 1) & 1;
+        if (!mbar_wait_ab(&bar_pf[sb], ph, err, &abort_s) || !mbar_wait_ab(&bar_vtf[sb], ph, err, &abort_s)) break;
+        tc_fence_after();
+        const uint32_t svt = smem_addr(smem + kDVTOff + sb * 32768);
+        const uint32_t sp = smem_addr(smem + kDPOff + sb * 4096);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          mma_f16(tmem + 32, sdesc_kmajor(svt + (k >> 2) * 16384 + (k & 3) * 32, 128),
+                  sdesc_kmajor(sp + (k >> 2) * 2048 + (k & 3) * 32, 128), kIdescDec,
+                  (jj > 0 || k > 0) ? 1u : 0u);
+        }
+        mma_commit(&bar_vte[sb]);
+        mma_commit(&bar_pe[sb]);
+        mma_commit(&bar_pv);
+        if (jj == n - 1) mma_commit(&bar_done);
+      }
+    }
+  } else if (warp >= 6) {
+    // ---------------- converters: V page (e4m3, [key][d]) -> V^T f16 image
+    const int ct = tid - 192;
+    for (int jj = 0; jj < n; ++jj) {
+      const int s = jj % kDecStages, sb = jj & 1;
+      if (!mbar_wait_ab(&bar_kvf[s], (jj / kDecStages) & 1, err, &abort_s)) break;
+      if (!mbar_wait_ab(&bar_vte[sb], ((jj >> 1) & 1) ^ 1, err, &abort_s)) break;
+      const uint8_t* vt = smem + kDVOff + s * 16384;
+      uint8_t* dst = smem + kDVTOff + sb * 32768;
+      const int nvalid = min(128, pos + 1 - int(sList[j0 + jj]) * 128);
+#pragma unroll 4
+      for (int x = ct; x < 2048; x += 128) {
+        const int d = x & 127, cc = (x >> 7) & 7, a = x >> 10;
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int k0 = a * 64 + cc * 8 + 2 * e;
+          const uint32_t lo = k0 < nvalid ? vt[k0 * 128 + d] : 0u;
+          const uint32_t hi = k0 + 1 < nvalid ? vt[(k0 + 1) * 128 + d] : 0u;
+          w[e] = e4m3x2_to_f16x2(uint16_t(lo | (hi << 8)));
+        }
+        *reinterpret_cast<uint4*>(dst + a * 16384 + swz_offset(d, cc, 128)) =
+            make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      fence_async_shared();
+      __syncwarp();
+      if (lane == 0) { mbar_arrive(&bar_vtf[sb]); mbar_arrive(&bar_kve[s]); }
+    }
+  } else {
+    // ---------------- softmax: thread = key lane of S^T and d lane of O^T
+    const int q4 = warp & 3;
+    const int key = q4 * 32 + lane;
+    const uint32_t lane_off = uint32_t(q4 * 32) << 16;
+    float m[16], mt[16], ls[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) { m[r] = -INFINITY; mt[r] = -INFINITY; ls[r] = 0.f; }
+    for (int jj = 0; jj < n; ++jj) {
+      const int sb = jj & 1;
+      const uint32_t ph = (jj >> 1) & 1;
+      const int blk = sList[j0 + jj];
+      const uint32_t rmask = sMask[j0 + jj];
+      const bool kvalid = blk * 128 + key <= pos;
+      mbar_wait_ab(&bar_sf[sb], ph, err, &abort_s);
+      tc_fence_after();
+      uint32_t v[16];
+      tmem_ld16(tmem + lane_off + sb * 16, v);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_se[sb]);
+      float x[16];
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        x[r] = (r < G && kvalid && ((rmask >> r) & 1u)) ? __uint_as_float(v[r]) * qk_scale2 : -INFINITY;
+        float mr = x[r];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mr = fmaxf(mr, __shfl_xor_sync(0xffffffffu, mr, o));
+        if (lane == 0) red[sb][q4][r] = mr;
+      }
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      float alpha[16];
+      bool need = false;
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        const float bm = fmaxf(fmaxf(red[sb][0][r], red[sb][1][r]), fmaxf(red[sb][2][r], red[sb][3][r]));
+        mt[r] = fmaxf(mt[r], bm);
+        alpha[r] = 1.0f;
+        if (bm > m[r] + kRescale) {
+          if (m[r] > -INFINITY) { alpha[r] = exp2f(m[r] - bm); need = true; }
+          m[r] = bm;
+        }
+      }
+      // P buffer sb is free once PV_{jj-2} is done (also bounds the pv parity below)
+      mbar_wait_ab(&bar_pe[sb], ph ^ 1, err, &abort_s);
+      if (need) {                       // uniform: every thread holds the same m
+        mbar_wait_ab(&bar_pv, (jj - 1) & 1, err, &abort_s);
+        tc_fence_after();
+        uint32_t o[16];
+        tmem_ld16(tmem + lane_off + 32, o);
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+          o[r] = __float_as_uint(__uint_as_float(o[r]) * alpha[r]);
+          ls[r] *= alpha[r];
+        }
+        tmem_st16(tmem + lane_off + 32, o);
+        tc_fence_before();
+      }
+      uint8_t* pb = smem + kDPOff + sb * 4096;
+      const uint32_t pofs = (key >> 6) * 2048;
+      const uint32_t cc = (key & 63) >> 3, e2 = (key & 7) * 2;
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        const float p = fast_exp2(x[r] - (m[r] == -INFINITY ? 0.f : m[r]));
+        ls[r] += p;
+        *reinterpret_cast<__half*>(pb + pofs + swz_offset(r, cc, 128) + e2) = __float2half_rn(p);
+      }
+      fence_async_shared();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_pf[sb]);
+    }
+    // chunk result: O^T columns (rows) for this thread's d lane, and row state
+    if (n > 0) mbar_wait_ab(&bar_done, 0, err, &abort_s);
+    tc_fence_after();
+    uint32_t o[16];
+    tmem_ld16(tmem + lane_off + 32, o);
+    const size_t base = (unit * max_chunks + c) * G;
+    for (int r = 0; r < G; ++r) part_o[(base + r) * 128 + key] = __uint_as_float(o[r]);
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      float sr = ls[r];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) sr += __shfl_xor_sync(0xffffffffu, sr, off);
+      if (lane == 0) lsum[q4][r] = sr;
+    }
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    if (tid - 64 < G) {
+      const int r = tid - 64;
+      part_s[base + r] = DecodePartial{m[r], lsum[0][r] + lsum[1][r] + lsum[2][r] + lsum[3][r], mt[r], 0.f};
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, 64);
+}
+
+// Merges the chunks of each (token, kv head) and applies the sink.
+__global__ void __launch_bounds__(256)
+decode_combine_kernel(const float* __restrict__ part_o, const DecodePartial* __restrict__ part_s,
+                      const int* __restrict__ n_chunks, const float* __restrict__ sink,
+                      float sink_scale2, float v_scale, int Hq, int Hkv, int max_chunks,
+                      uint16_t* __restrict__ out, float* __restrict__ max_logit,
+                      float* __restrict__ lse) {
+  const int t = blockIdx.x / Hkv, g = blockIdx.x % Hkv;
+  const int G = Hq / Hkv;
+  const size_t unit = size_t(t) * Hkv + g;
+  const int nch = n_chunks[unit];
+  for (int x = threadIdx.x; x < G * 128; x += blockDim.x) {
+    const int r = x >> 7, d = x & 127;
+    const int h = g * G + r;
+    float M = -INFINITY, mt = -INFINITY;
+    for (int c = 0; c < nch; ++c) {
+      const DecodePartial ps = part_s[(unit * max_chunks + c) * G + r];
+      M = fmaxf(M, ps.m);
+      mt = fmaxf(mt, ps.m_true);
+    }
+    const float sig2 = sink != nullptr ? sink_scale2 * __ldg(sink + h) : -INFINITY;
+    const float Mz = fmaxf(M, sig2);
+    float Z = (sig2 == -INFINITY) ? 0.f : exp2f(sig2 - Mz), acc = 0.f;
+    for (int c = 0; c < nch; ++c) {
+      const size_t k = (unit * max_chunks + c) * G + r;
+      const DecodePartial ps = part_s[k];
+      if (ps.m == -INFINITY) continue;
+      const float f = exp2f(ps.m - Mz);
+      Z += ps.l * f;
+      acc += part_o[k * 128 + d] * f;
+    }
+    const float o = Z > 0.f ? acc / Z * v_scale : 0.f;
+    out[(size_t(t) * Hq + h) * 128 + d] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
+    if (d == 0) {
+      max_logit[size_t(t) * Hq + h] = mt * kLn2;
+      lse[size_t(t) * Hq + h] = Z > 0.f ? (Mz + log2f(Z)) * kLn2 : -INFINITY;
+    }
+  }
+}
+
+cudaError_t launch_decode(const AttnArgs& a, cudaStream_t stream, const char** why) {
+  const int G = a.Hq / a.Hkv, hpi = a.Hq / a.Hidx;
+  const int n_idx = (G + hpi - 1) / hpi + 1;
+  const int mc = dec_max_chunks(n_idx, a.topk_k, a.max_pages);
+  const size_t units = size_t(a.T) * a.Hkv * mc * G;
+  uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+  float* part_o = reinterpret_cast<float*>(ws);
+  DecodePartial* part_s = reinterpret_cast<DecodePartial*>(ws + align256(units * 128 * sizeof(float)));
+  int* n_chunks = reinterpret_cast<int*>(ws + align256(units * 128 * sizeof(float)) +
+                                         align256(units * sizeof(DecodePartial)));
+  CUtensorMap tm_q, tm_k, tm_v;
+  {
+    const uint64_t dims[2] = {128, uint64_t(a.T) * a.Hq};
+    const uint64_t strides[1] = {128};
+    const uint32_t box[2] = {128, 16};
+    if (!encode_tensor_map(&tm_q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.q, dims, strides, box,
+                           CU_TENSOR_MAP_SWIZZLE_128B, why))
+      return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[2] = {128, uint64_t(a.num_pages) * a.Hkv * 128};
+    const uint64_t strides[1] = {128};
+    const uint32_t box[2] = {128, 128};
+    if (!encode_tensor_map(&tm_k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.k_cache, dims, strides, box,
+                           CU_TENSOR_MAP_SWIZZLE_128B, why) ||
+        !encode_tensor_map(&tm_v, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.v_cache, dims, strides, box,
+                           CU_TENSOR_MAP_SWIZZLE_NONE, why))
+      return cudaErrorInvalidValue;
+  }
+  cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecodeSmem);
+  if (e != cudaSuccess) return e;
+  attn_decode_kernel<<<a.T * a.Hkv * mc, 320, kDecodeSmem, stream>>>(
+      tm_q, tm_k, tm_v, a.page_table, a.seq_lens, a.cu_q, a.topk, a.c_qk * kLog2e, a.B, a.T, a.Hq,
+      a.Hkv, a.Hidx, a.topk_k, a.max_pages, a.num_pages, mc, part_o, part_s, n_chunks, a.err);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  decode_combine_kernel<<<a.T * a.Hkv, 256, 0, stream>>>(part_o, part_s, n_chunks, a.sink,
+                                                         a.c_sink * kLog2e, a.v_scale, a.Hq, a.Hkv,
+                                                         mc, a.out, a.max_logit, a.lse);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
-size_t attn_workspace_bytes(int B, int T, int max_q_len, int Hkv, int D, int max_pages) {
-  (void)D;
-  if (max_q_len <= 1) return 0;
+size_t attn_workspace_bytes(int B, int T, int max_q_len, int Hq, int Hkv, int Hidx, int topk,
+                            int max_pages) {
+  if (max_q_len <= 1) {
+    const int G = Hq / Hkv, hpi = Hq / Hidx;
+    const int n_idx = (G + hpi - 1) / hpi + 1;          // index heads one kv group can touch
+    const int mc = dec_max_chunks(n_idx, topk, max_pages);
+    const size_t units = size_t(T) * Hkv * mc * G;
+    return align256(units * 128 * sizeof(float)) + align256(units * sizeof(DecodePartial)) +
+           align256(size_t(T) * Hkv * sizeof(int)) + 256;
+  }
   const size_t img = size_t(B) * max_pages * Hkv * 32768;
   return img + align256(size_t(T + B + 1) * sizeof(TileInfo)) + 256;
 }
@@ -383,11 +805,8 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream, const cha
     *why = "max_pages must be <= 2048";
     return cudaErrorNotSupported;
   }
-  if (a.max_q_len == 1) {
-    *why = "decode attention not built yet";
-    return cudaErrorNotSupported;
-  }
   const int G = a.Hq / a.Hkv;
+  if (a.max_q_len == 1) return launch_decode(a, stream, why);
   const int toks = 128 / G;
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   const size_t img_bytes = size_t(a.B) * a.max_pages * a.Hkv * 32768;

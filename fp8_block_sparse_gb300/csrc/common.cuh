@@ -74,6 +74,24 @@ MSA_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* err) {
   }
 }
 
+// As mbar_wait, but returns false at once when *abort is set, and sets it
+// when its own limit runs out: after the first timeout every role of the CTA
+// stops waiting and drains its loop quickly.
+MSA_DEV bool mbar_wait_ab(uint64_t* bar, uint32_t parity, unsigned* err, volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (*abort) return false;
+    for (int i = 0; i < 256; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      atomicOr(err, MSA_DEVERR_TIMEOUT);
+      *abort = 1;
+      return false;
+    }
+  }
+}
+
 // ---------------------------------------------------------------- TMA
 MSA_DEV void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

@@ -66,7 +66,8 @@ struct AttnArgs {
   unsigned* err;
 };
 cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream, const char** why);
-size_t attn_workspace_bytes(int B, int T, int max_q_len, int Hkv, int D, int max_pages);
+size_t attn_workspace_bytes(int B, int T, int max_q_len, int Hq, int Hkv, int Hidx, int topk,
+                            int max_pages);
 
 // Step (c), sparse MLA.
 struct MlaArgs {

@@ -147,7 +147,8 @@ msa_status msa_index_topk(const uint8_t* idx_q, const uint8_t* idx_k_cache,
                           void* workspace, size_t workspace_bytes, msa_stream_t stream);
 
 /* Bytes of device workspace msa_sparse_attn_fwd needs for these sizes. */
-size_t msa_sparse_attn_workspace_size(int B, int T, int max_q_len, int Hkv, int D, int max_pages);
+size_t msa_sparse_attn_workspace_size(int B, int T, int max_q_len, int Hq, int Hkv, int Hidx,
+                                      int topk, int max_pages);
 
 /*
  * Step (c): GQA sparse attention over the selected blocks.
@@ -169,8 +170,10 @@ size_t msa_sparse_attn_workspace_size(int B, int T, int max_q_len, int Hkv, int 
  * topk_indices: device int32 [Hidx][T][topk], ascending, -1 padded
  * sink:         device fp32 [Hq] or NULL
  * out:          device bf16 [T][Hq][D];  max_logit, lse: device fp32 [T][Hq]
- * workspace:    device, >= msa_sparse_attn_workspace_size(...) bytes
- *               (0 for decode), 256-byte aligned.
+ * workspace:    device, >= msa_sparse_attn_workspace_size(...) bytes,
+ *               256-byte aligned; contents on entry are ignored. Prefill
+ *               keeps f16 V^T page images there, decode its per-chunk
+ *               partial softmax states.
  * Supported: D == 128; Hq % Hkv == 0, Hq % Hidx == 0, Hq/Hkv a power of two
  * <= 16; 1 <= topk <= 64.
  */
