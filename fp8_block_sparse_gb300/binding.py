@@ -43,6 +43,8 @@ _SIGNATURES = {
     "msa_version": ([], _I),
     "msa_last_error_string": ([], ctypes.c_char_p),
     "msa_check_errors": ([_P], _I),
+    "msa_profile_enable": ([_I], _I),
+    "msa_profile_last_ms": ([_FP], _I),
     "msa_quant_fp8": ([_P, _I, _I64, _I64, _I64, _P, _I, _I64, _FP, _P], _I),
     "msa_index_topk_workspace_size": ([_I, _I, _I], _SZ),
     "msa_index_topk": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P], _I),
@@ -102,6 +104,18 @@ def _dev(t: torch.Tensor, name: str, dtype=None) -> None:
 def check_errors(stream: Optional[torch.cuda.Stream] = None) -> None:
     """Synchronise and raise if a kernel recorded a device-side data error."""
     _check(load().msa_check_errors(_stream(stream)))
+
+
+def profile_enable(on: bool = True) -> None:
+    """Record events around the main attention kernel of each call (instrumentation)."""
+    _check(load().msa_profile_enable(1 if on else 0))
+
+
+def profile_last_ms() -> float:
+    """Elapsed ms of the most recently profiled main attention kernel."""
+    v = ctypes.c_float(0.0)
+    _check(load().msa_profile_last_ms(ctypes.byref(v)))
+    return float(v.value)
 
 
 def quant_fp8(x: torch.Tensor, scale: Optional[float] = None, out: Optional[torch.Tensor] = None,

@@ -38,6 +38,8 @@ std::mutex g_mutex;
 unsigned* g_err_ptr[kMaxDevices] = {};
 int g_sms[kMaxDevices] = {};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+bool g_profile = false;
+cudaEvent_t g_ev[kMaxDevices][2] = {};
 
 int current_device() {
   int d = 0;
@@ -87,6 +89,22 @@ int num_sms() {
   return g_sms[d];
 }
 
+void profile_mark(cudaStream_t stream, int which) {
+  if (!g_profile) return;
+  const int d = current_device();
+  if (d < 0) return;
+  cudaEvent_t ev;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (g_ev[d][0] == nullptr) {
+      if (cudaEventCreate(&g_ev[d][0]) != cudaSuccess || cudaEventCreate(&g_ev[d][1]) != cudaSuccess)
+        return;
+    }
+    ev = g_ev[d][which];
+  }
+  cudaEventRecord(ev, stream);
+}
+
 bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank, const void* base,
                        const uint64_t* dims, const uint64_t* strides_bytes, const uint32_t* box,
                        CUtensorMapSwizzle swizzle, const char** why) {
@@ -132,6 +150,22 @@ extern "C" {
 int msa_version(void) { return 100; }
 
 const char* msa_last_error_string(void) { return g_last_error.c_str(); }
+
+msa_status msa_profile_enable(int enable) {
+  g_profile = enable != 0;
+  return MSA_OK;
+}
+
+msa_status msa_profile_last_ms(float* ms) {
+  if (ms == nullptr) return fail(MSA_ERR_INVALID_ARG, "msa_profile_last_ms: null pointer");
+  const int d = current_device();
+  if (d < 0 || g_ev[d][0] == nullptr)
+    return fail(MSA_ERR_INVALID_ARG, "msa_profile_last_ms: nothing was profiled on this device");
+  cudaError_t e = cudaEventSynchronize(g_ev[d][1]);
+  if (e == cudaSuccess) e = cudaEventElapsedTime(ms, g_ev[d][0], g_ev[d][1]);
+  if (e != cudaSuccess) return cuda_fail(e, "msa_profile_last_ms");
+  return MSA_OK;
+}
 
 msa_status msa_check_errors(msa_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));

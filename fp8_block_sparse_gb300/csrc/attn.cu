@@ -773,9 +773,11 @@ cudaError_t launch_decode(const AttnArgs& a, cudaStream_t stream, const char** w
   }
   cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecodeSmem);
   if (e != cudaSuccess) return e;
+  profile_mark(stream, 0);
   attn_decode_kernel<<<a.T * a.Hkv * mc, 320, kDecodeSmem, stream>>>(
       tm_q, tm_k, tm_v, a.page_table, a.seq_lens, a.cu_q, a.topk, a.c_qk * kLog2e, a.B, a.T, a.Hq,
       a.Hkv, a.Hidx, a.topk_k, a.max_pages, a.num_pages, mc, part_o, part_s, n_chunks, a.err);
+  profile_mark(stream, 1);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   decode_combine_kernel<<<a.T * a.Hkv, 256, 0, stream>>>(part_o, part_s, n_chunks, a.sink,
@@ -840,10 +842,12 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream, const cha
   e = cudaFuncSetAttribute(attn_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrefillSmem);
   if (e != cudaSuccess) return e;
   const int grid = ((a.T + toks - 1) / toks + a.B) * a.Hkv;
+  profile_mark(stream, 0);
   attn_prefill_kernel<<<grid, 192, kPrefillSmem, stream>>>(
       tm_q, tm_k, ws, a.page_table, tiles, n_tiles, a.topk, a.sink, a.c_qk * kLog2e,
       a.c_sink * kLog2e, a.v_scale, a.T, a.Hq, a.Hkv, a.Hidx, toks, a.topk_k, a.max_pages,
       a.num_pages, a.out, a.max_logit, a.lse, a.err);
+  profile_mark(stream, 1);
   return cudaGetLastError();
 }
 

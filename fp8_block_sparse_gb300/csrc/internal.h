@@ -24,6 +24,10 @@ bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank, co
 
 int num_sms();
 
+// Instrumentation: records the start (which = 0) or stop (which = 1) event
+// around a main attention kernel when profiling is enabled; no-op otherwise.
+void profile_mark(cudaStream_t stream, int which);
+
 // Step (a).
 cudaError_t launch_quant(const void* x, bool bf16, int64_t rows, int64_t cols, int64_t x_stride,
                          uint8_t* out, int64_t out_stride, float s_inv, cudaStream_t stream);

@@ -85,6 +85,18 @@ int msa_version(void);
 const char* msa_last_error_string(void);
 
 /*
+ * Instrumentation, not part of the computation. While enabled (enable != 0),
+ * every msa_sparse_attn_fwd and msa_sparse_mla_fwd call records a pair of
+ * CUDA events on its stream around its main attention kernel (the prefill,
+ * decode or MLA kernel; not the small planning, conversion or combine
+ * kernels). msa_profile_last_ms waits for the most recent stop event and
+ * returns the elapsed milliseconds. Disabled by default; the events belong to
+ * the library (one pair per device). Do not enable during graph capture.
+ */
+msa_status msa_profile_enable(int enable);
+msa_status msa_profile_last_ms(float* ms);
+
+/*
  * Synchronises `stream`, then reads and clears the device error word.
  * Returns MSA_OK, MSA_ERR_DATA (bad page id / index seen by a kernel) or
  * MSA_ERR_TIMEOUT (a bounded device wait gave up), or MSA_ERR_CUDA.
