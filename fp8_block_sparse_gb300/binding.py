@@ -48,6 +48,7 @@ _SIGNATURES = {
     "msa_quant_fp8": ([_P, _I, _I64, _I64, _I64, _P, _I, _I64, _FP, _P], _I),
     "msa_index_topk_workspace_size": ([_I, _I, _I], _SZ),
     "msa_index_topk": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P], _I),
+    "msa_index_topk_noalloc": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P], _I),
     "msa_sparse_attn_workspace_size": ([_I, _I, _I, _I, _I, _I, _I, _I], _SZ),
     "msa_sparse_attn_fwd": ([_P, _P, _P, _P, _P, _P, _P, _P, _F, _FP, _FP, _FP,
                              _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _SZ, _P], _I),
@@ -163,6 +164,27 @@ def index_topk(idx_q: torch.Tensor, idx_k_cache: torch.Tensor, page_table: torch
     _check(lib.msa_index_topk(_ptr(idx_q), _ptr(idx_k_cache), _ptr(page_table), _ptr(seq_lens),
                               _ptr(cu_q), B, T, max_q_len, Hidx, D, topk, num_pages, max_pages,
                               _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out
+
+
+def index_topk_noalloc(idx_q: torch.Tensor, idx_k_cache: torch.Tensor, page_table: torch.Tensor,
+                       seq_lens: torch.Tensor, cu_q: torch.Tensor, topk: int, max_q_len: int,
+                       out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """index_topk without a workspace: the library's fixed device scratch is
+    used instead (for callers that may not allocate device memory)."""
+    lib = load()
+    T, Hidx, D = idx_q.shape
+    num_pages = idx_k_cache.shape[0]
+    B, max_pages = page_table.shape
+    for t, n in ((idx_q, "idx_q"), (idx_k_cache, "idx_k_cache")):
+        _dev(t, n, torch.uint8)
+    for t, n in ((page_table, "page_table"), (seq_lens, "seq_lens"), (cu_q, "cu_q")):
+        _dev(t, n, torch.int32)
+    if out is None:
+        out = torch.empty((Hidx, T, topk), dtype=torch.int32, device=idx_q.device)
+    _check(lib.msa_index_topk_noalloc(_ptr(idx_q), _ptr(idx_k_cache), _ptr(page_table), _ptr(seq_lens),
+                                      _ptr(cu_q), B, T, max_q_len, Hidx, D, topk, num_pages, max_pages,
+                                      _ptr(out), _stream(stream)))
     return out
 
 

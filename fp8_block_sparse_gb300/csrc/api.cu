@@ -65,6 +65,8 @@ bool read_scale(const float* s, float* out, const char* name) {
 
 }  // namespace
 
+void set_last_error(const std::string& msg) { g_last_error = msg; }
+
 unsigned* device_error_word() {
   const int d = current_device();
   if (d < 0) return nullptr;

@@ -7,11 +7,16 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <string>
+
 namespace msa {
 
 // Bits of the device error word.
 constexpr unsigned MSA_DEVERR_DATA = 1u;     // bad page id / index seen by a kernel
 constexpr unsigned MSA_DEVERR_TIMEOUT = 2u;  // a bounded wait gave up
+
+// Sets the message msa_last_error_string() returns on this thread.
+void set_last_error(const std::string& msg);
 
 // Device address of this device's error word (set up once per device).
 unsigned* device_error_word();

@@ -158,6 +158,33 @@ msa_status msa_index_topk(const uint8_t* idx_q, const uint8_t* idx_k_cache,
                           int topk, int num_pages, int max_pages, int32_t* topk_indices,
                           void* workspace, size_t workspace_bytes, msa_stream_t stream);
 
+/*
+ * msa_index_topk for callers that cannot allocate device memory. The pages
+ * have no counterpart to this entry point; it exists for this library's users.
+ *
+ * Same arguments, results and errors as msa_index_topk, without the
+ * workspace: the scratch lives in one fixed 8 MiB array in the library's
+ * device image (held on every GPU that loads the library until exit). Meant
+ * for callers that get only their input and output pointers from a host
+ * engine with no workspace hook, or that reserve all device memory up front
+ * and may not call cudaMalloc afterwards. It calls no allocator.
+ * - Sizes whose scratch (msa_index_topk_workspace_size(T, Hidx, max_pages))
+ *   exceeds 8 MiB are rejected with MSA_ERR_WORKSPACE before any launch; the
+ *   paged-decode workload (128 sequences x 4 index heads x 512 pages, 1 MiB)
+ *   and short prefills fit, long prefills need msa_index_topk.
+ * - The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current); make that first call
+ *   before any stream capture.
+ * - Every call uses the same array and leaves its contents behind; calls
+ *   that may run at the same time on the GPU (unordered streams) race on it
+ *   and must be serialised by the caller. No contents need to start at zero.
+ */
+msa_status msa_index_topk_noalloc(const uint8_t* idx_q, const uint8_t* idx_k_cache,
+                                  const int32_t* page_table, const int32_t* seq_lens,
+                                  const int32_t* cu_q, int B, int T, int max_q_len, int Hidx,
+                                  int D, int topk, int num_pages, int max_pages,
+                                  int32_t* topk_indices, msa_stream_t stream);
+
 /* Bytes of device workspace msa_sparse_attn_fwd needs for these sizes. */
 size_t msa_sparse_attn_workspace_size(int B, int T, int max_q_len, int Hq, int Hkv, int Hidx,
                                       int topk, int max_pages);
