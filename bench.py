@@ -53,6 +53,7 @@ def parse():
     p.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU oracle sample budget")
     p.add_argument("--no-e2e", action="store_true", help="skip the end-to-end measurement")
+    p.add_argument("--no-mla", action="store_true", help="skip the sparse-MLA measurement")
     p.add_argument("--workload", default=WORKLOAD, choices=["prefill32k", "prefill8k", "tiny"],
                    help="prefill workload of the step (the benchmark line uses prefill32k)")
     return p.parse_args()
@@ -268,6 +269,51 @@ def decode_bytes(st):
     kv_bytes = union * 2.0 * 128 * cfg.D
     small = w.T * (cfg.Hq * cfg.D * 3 + cfg.Hidx * cfg.d_idx * 3 + cfg.Hq * 2 * cfg.D + 8 * cfg.Hq)
     return idx_bytes + kv_bytes + small, kv_bytes, union
+
+
+def mla_measure(msa, wl, dev, steps, flush, pk):
+    """Sparse-MLA prefill workload: quantise Q + MLA kernel per step."""
+    import numpy as np
+    import torch
+    w = wl.make_mla(wl.CONFIGS["mla"])
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    q = bf(w.q)
+    kv8 = msa.quant_fp8(bf(w.kv), w.scales["kv"])
+    idx, tl, sink = t(w.indices), t(w.topk_length), t(w.sink)
+    T, H = w.q.shape[0], w.q.shape[1]
+    q8 = torch.empty(w.q.shape, dtype=torch.uint8, device=dev)
+    o = torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev)
+    ml = torch.empty((T, H), dtype=torch.float32, device=dev)
+    ls = torch.empty((T, H), dtype=torch.float32, device=dev)
+
+    def step():
+        msa.quant_fp8(q, w.scales["q"], out=q8)
+        msa.sparse_mla_fwd(q8, kv8, idx, tl, sink, w.sm_scale, w.scales["q"], w.scales["kv"],
+                           out=o, max_logits=ml, lse=ls)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    ms, kern = [], []
+    for _ in range(steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        step()
+        b.record()
+        kern.append(msa.profile_last_ms())
+        torch.cuda.synchronize()
+        ms.append(a.elapsed_time(b))
+    msa.check_errors()
+    flops = float(np.sum(w.topk_length.astype(np.float64))) * H * (2 * 576 + 2 * 512)
+    k = statistics.mean(kern)
+    fp8_peak = 2.0 * pk["bf16_tflops"]
+    return {"workload": "mla", "queries": T, "heads": H, "ms_per_step": statistics.mean(ms),
+            "tokens_per_s": T / (statistics.mean(ms) / 1e3),
+            "kernel": "mla_prefill_kernel", "kernel_ms": k, "tflops_algorithmic": flops / (k / 1e3) / 1e12,
+            "frac_of_fp8_peak": flops / (k / 1e3) / 1e12 / fp8_peak, "algorithmic_flop": flops,
+            "peak_basis": f"{pk['source']} bf16 burst x2"}
 
 
 # ----------------------------------------------------------------- CPU oracle
@@ -504,6 +550,11 @@ def native_arm(args):
                   "peak_hbm_gbs": pk["hbm_gbs"], "peak_basis": pk["source"]}
         del ds
 
+    mla = None
+    if not args.no_mla:
+        torch.cuda.empty_cache()
+        mla = mla_measure(msa, wl, dev, args.steps, flush, pk)
+
     # ---- CPU oracle on a bounded sample (rank 0, N = 1 only)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -526,6 +577,7 @@ def native_arm(args):
             "breakdown_ms": {"quant": quant_ms, "index_topk": index_ms, "attention_call": attn_call_ms,
                              "attention_kernel": kern_ms},
             "decode": decode,
+            "mla": mla,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": LAUNCHES_PREFILL * args.steps,

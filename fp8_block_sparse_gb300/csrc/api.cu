@@ -360,8 +360,8 @@ msa_status msa_sparse_mla_fwd(const uint8_t* q, const uint8_t* kv, const int32_t
   if (T == 0) return MSA_OK;
   if (!q || !kv || !indices || !out || !max_logits || !lse)
     return fail(MSA_ERR_INVALID_ARG, std::string(fn) + ": null pointer");
-  if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(out, 16))
-    return fail(MSA_ERR_INVALID_ARG, std::string(fn) + ": q/kv/out must be 16-byte aligned");
+  if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(out, 16) || !aligned(indices, 16))
+    return fail(MSA_ERR_INVALID_ARG, std::string(fn) + ": q/kv/indices/out must be 16-byte aligned");
   MlaArgs a{};
   a.q = q;
   a.kv = kv;

@@ -1,7 +1,334 @@
+// mla.cu -- step (c), sparse-MLA prefill: MQA of 128 query heads over one
+// latent kv head, each query attending to its own list of kv rows.
+//
+// What is computed (sglang PR 25751 page, key source excerpt of
+// sparse_mla_q8kv8_prefill_fwd; scale rules of sglang PR 30971 page,
+// implementation step 3): query t attends to kv[indices[t, j]] for
+// j < topk_length[t] (negative entries skipped); V is the first 512 columns
+// of the same rows; with c = sm_scale * q_scale,
+//   l_j = c * kv_scale * (q[t,h] . kv[idx_j])      (576-dim dot)
+//   out = kv_scale * sum_j e^{l_j} kv[idx_j, :512] / (sum_j e^{l_j} + e^{c*sink[h]})
+//   max_logits = max_j l_j,  lse = ln(sum_j e^{l_j} + e^{c*sink[h]}).
+//
+// GB300 design. The 128 heads of one query share its index list, so they are
+// the M = 128 rows of every MMA. A CTA owns one query token and one half of
+// d_v: the full 128 x 512 fp32 O would take all 512 TMEM columns, leaving
+// none for S, so each half keeps a 256-column O and recomputes S (the QK^T
+// part is 53% of the flops; duplicating it costs 1.5x the MMA work of one CTA
+// per token, and the two halves run as separate CTAs on different SMs).
+// Per 64-key chunk of the index list:
+//   gather   four producer warps copy the 64 kv rows (576 B each) with 16-byte
+//            cp.async into a K-major tile: four 128-byte swizzled regions plus
+//            one 64-byte swizzled region for the last 64 columns; invalid
+//            entries become zero rows (and are masked);
+//   S = Q K^T  tcgen05 e4m3, M=128, N=64, K=576 (18 MMAs), double-buffered TMEM;
+//   V^T      the same warps turn this CTA's 256 V columns of the tile into an
+//            f16 V^T operand (rows = d, K = keys);
+//   P        one thread per head row: online softmax with lazy rescale, P in
+//            f16 (e4m3 P costs ~2.5% relative error on flat rows);
+//   O += P V tcgen05 kind::f16, M=128, N=256, K=64.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "common.cuh"
 #include "internal.h"
+
 namespace msa {
-cudaError_t launch_sparse_mla(const MlaArgs&, cudaStream_t, const char** why) {
-  *why = "not built yet";
-  return cudaErrorNotSupported;
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescale = 8.0f;
+constexpr int kDqk = 576, kDv = 512, kChunkKeys = 64;
+
+// shared memory (byte offsets from a 1024-aligned base)
+constexpr int kQOff = 0;            // 128 x 576 e4m3: 4 x 16 KB (SW128) + 8 KB (SW64)
+constexpr int kQTail = 65536;
+constexpr int kKOff = 73728;        // 2 stages x 36 KB: 4 x 8 KB (SW128) + 4 KB (SW64)
+constexpr int kKStage = 36864;
+constexpr int kKTail = 32768;       // offset of the SW64 region inside a stage
+constexpr int kVTOff = 147456;      // 256 x 64 f16 V^T (one 128-byte swizzle column)
+constexpr int kPOff = 180224;       // 2 x (128 x 64 f16)
+constexpr int kMlaSmem = 212992 + 1024;
+
+constexpr uint32_t kIdescQK = idesc_f32(128, 64);
+constexpr uint32_t kIdescPV = idesc_f32(128, 256);
+
+__global__ void __launch_bounds__(288, 1)
+mla_prefill_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_constant__ CUtensorMap tm_q64,
+                   const uint8_t* __restrict__ kv, const int32_t* __restrict__ indices,
+                   const int32_t* __restrict__ topk_length, const float* __restrict__ sink,
+                   float qk_scale2, float sink_scale2, float v_scale, int T, int S_kv, int topk,
+                   uint16_t* __restrict__ out, float* __restrict__ max_logits,
+                   float* __restrict__ lse, unsigned* err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  __shared__ uint64_t bar_q, bar_kf[2], bar_ke[2], bar_sf[2], bar_se[2], bar_pf[2], bar_pe[2],
+      bar_vtf, bar_vte, bar_pv, bar_done;
+  __shared__ uint32_t tmem_base_s;
+  __shared__ int abort_s;
+
+  const int t = blockIdx.x >> 1, hf = blockIdx.x & 1;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  int len = topk_length != nullptr ? topk_length[t] : topk;
+  len = max(0, min(len, topk));
+  const int nch = (len + kChunkKeys - 1) / kChunkKeys;
+  const int32_t* idx_row = indices + size_t(t) * topk;
+
+  if (tid == 0) {
+    abort_s = 0;
+    mbar_init(&bar_q, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bar_kf[s], 1); mbar_init(&bar_ke[s], 5);
+      mbar_init(&bar_sf[s], 1); mbar_init(&bar_se[s], 4);
+      mbar_init(&bar_pf[s], 4); mbar_init(&bar_pe[s], 1);
+    }
+    mbar_init(&bar_vtf, 4); mbar_init(&bar_vte, 1);
+    mbar_init(&bar_pv, 1); mbar_init(&bar_done, 1);
+    fence_barrier_init();
+  }
+  if (warp == 0) { tmem_alloc(&tmem_base_s, 512); tmem_relinquish(); }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_s;          // S buffers at cols 0 and 64; O at 256
+
+  if (warp == 0) {
+    // ---------------- Q (one TMA batch) and MMA issue
+    if (lane == 0 && nch > 0) {
+      mbar_arrive_expect_tx(&bar_q, 128 * kDqk);
+      for (int r = 0; r < 4; ++r) tma_load_2d(smem + kQOff + r * 16384, &tm_q128, &bar_q, r * 128, t * 128);
+      tma_load_2d(smem + kQTail, &tm_q64, &bar_q, 512, t * 128);
+      if (mbar_wait_ab(&bar_q, 0, err, &abort_s)) {
+        const uint32_t sq = smem_addr(smem + kQOff);
+        auto issue_s = [&](int j) -> bool {
+          const int s = j & 1;
+          const uint32_t ph = (j >> 1) & 1;
+          if (!mbar_wait_ab(&bar_kf[s], ph, err, &abort_s)) return false;
+          if (!mbar_wait_ab(&bar_se[s], ph ^ 1, err, &abort_s)) return false;
+          tc_fence_after();
+          const uint32_t sk = smem_addr(smem + kKOff + s * kKStage);
+#pragma unroll
+          for (int k = 0; k < 16; ++k)
+            mma_e4m3(tmem + s * 64, sdesc_kmajor(sq + (k >> 2) * 16384 + (k & 3) * 32, 128),
+                     sdesc_kmajor(sk + (k >> 2) * 8192 + (k & 3) * 32, 128), kIdescQK, k > 0);
+#pragma unroll
+          for (int k = 0; k < 2; ++k)
+            mma_e4m3(tmem + s * 64, sdesc_kmajor(sq + kQTail + k * 32, 64),
+                     sdesc_kmajor(sk + kKTail + k * 32, 64), kIdescQK, 1u);
+          mma_commit(&bar_ke[s]);
+          mma_commit(&bar_sf[s]);
+          return true;
+        };
+        bool ok = issue_s(0);
+        for (int j = 0; ok && j < nch; ++j) {
+          if (j + 1 < nch && !(ok = issue_s(j + 1))) break;
+          const int s = j & 1;
+          const uint32_t ph = (j >> 1) & 1;
+          if (!mbar_wait_ab(&bar_pf[s], ph, err, &abort_s) || !mbar_wait_ab(&bar_vtf, j & 1, err, &abort_s)) break;
+          tc_fence_after();
+          const uint32_t sp = smem_addr(smem + kPOff + s * 16384), svt = smem_addr(smem + kVTOff);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_f16(tmem + 256, sdesc_kmajor(sp + k * 32, 128), sdesc_kmajor(svt + k * 32, 128), kIdescPV,
+                    (j > 0 || k > 0) ? 1u : 0u);
+          mma_commit(&bar_vte);
+          mma_commit(&bar_pe[s]);
+          mma_commit(&bar_pv);
+          if (j == nch - 1) mma_commit(&bar_done);
+        }
+      }
+    }
+  } else if (warp <= 4) {
+    // ---------------- producers: gather chunk j, convert chunk j-1
+    const int pt = tid - 32;
+    const int r = pt >> 1, part = pt & 1;
+    for (int j = 0; j <= nch; ++j) {
+      if (j < nch) {
+        const int s = j & 1;
+        mbar_wait_ab(&bar_ke[s], ((j >> 1) & 1) ^ 1, err, &abort_s);
+        const int key = j * kChunkKeys + r;
+        int idx = key < len ? __ldg(idx_row + key) : -1;
+        if (idx >= S_kv) { atomicOr(err, MSA_DEVERR_DATA); idx = -1; }
+        uint8_t* stage = smem + kKOff + s * kKStage;
+        const uint8_t* src = kv + size_t(idx < 0 ? 0 : idx) * kDqk;
+#pragma unroll
+        for (int cc = 0; cc < 18; ++cc) {
+          const int c = part * 18 + cc;
+          uint8_t* dst = c < 32 ? stage + (c >> 3) * 8192 + swz_offset(r, c & 7, 128)
+                                : stage + kKTail + swz_offset(r, c - 32, 64);
+          if (idx >= 0) cp_async16(dst, src + c * 16);
+          else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        cp_async_commit();
+      }
+      if (j >= 1) {
+        const int jp = j - 1, sp = jp & 1;
+        if (j < nch) cp_async_wait<1>(); else cp_async_wait<0>();
+        fence_async_shared();
+        asm volatile("bar.sync 2, 128;" ::: "memory");        // chunk jp has landed
+        if (pt == 0) mbar_arrive(&bar_kf[sp]);
+        // V^T for this CTA's d_v half: row d (0..255), 16-byte chunk = 8 keys
+        mbar_wait_ab(&bar_vte, (jp & 1) ^ 1, err, &abort_s);
+        const uint8_t* stage = smem + kKOff + sp * kKStage;
+        uint8_t* vt = smem + kVTOff;
+#pragma unroll 2
+        for (int x = pt; x < 256 * 8; x += 128) {
+          const int dl = x & 255, c8 = x >> 8;
+          const int d = hf * 256 + dl;
+          const uint8_t* col = stage + (d >> 7) * 8192;
+          const int dc = (d & 127) >> 4, db = d & 15;
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int k0 = c8 * 8 + 2 * e;
+            const uint32_t lo = col[swz_offset(k0, dc, 128) + db];
+            const uint32_t hi = col[swz_offset(k0 + 1, dc, 128) + db];
+            w[e] = e4m3x2_to_f16x2(uint16_t(lo | (hi << 8)));
+          }
+          *reinterpret_cast<uint4*>(vt + swz_offset(dl, c8, 128)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        fence_async_shared();
+        __syncwarp();
+        if (lane == 0) { mbar_arrive(&bar_vtf); mbar_arrive(&bar_ke[sp]); }
+      }
+    }
+  } else {
+    // ---------------- softmax: thread = head row (TMEM lane)
+    const int q4 = warp & 3;
+    const int row = q4 * 32 + lane;
+    const uint32_t lane_off = uint32_t(q4 * 32) << 16;
+    float m = -INFINITY, m_true = -INFINITY, l = 0.f;
+    for (int j = 0; j < nch; ++j) {
+      const int s = j & 1;
+      const uint32_t ph = (j >> 1) & 1;
+      uint64_t valid = 0;
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        const int4 iv = __ldg(reinterpret_cast<const int4*>(idx_row + j * kChunkKeys) + q);
+        const int base = j * kChunkKeys + q * 4;
+        valid |= uint64_t((iv.x >= 0 && iv.x < S_kv && base + 0 < len) ? 1 : 0) << (q * 4 + 0);
+        valid |= uint64_t((iv.y >= 0 && iv.y < S_kv && base + 1 < len) ? 1 : 0) << (q * 4 + 1);
+        valid |= uint64_t((iv.z >= 0 && iv.z < S_kv && base + 2 < len) ? 1 : 0) << (q * 4 + 2);
+        valid |= uint64_t((iv.w >= 0 && iv.w < S_kv && base + 3 < len) ? 1 : 0) << (q * 4 + 3);
+      }
+      mbar_wait_ab(&bar_sf[s], ph, err, &abort_s);
+      tc_fence_after();
+      float x[64];
+#pragma unroll
+      for (int c = 0; c < 64; c += 32) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_off + s * 64 + c, v);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) x[c + e] = __uint_as_float(v[e]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_se[s]);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        x[c] = ((valid >> c) & 1) ? x[c] * qk_scale2 : -INFINITY;
+        mx = fmaxf(mx, x[c]);
+      }
+      m_true = fmaxf(m_true, mx);
+      mbar_wait_ab(&bar_pe[s], ph ^ 1, err, &abort_s);      // PV_{j-2} done: P buffer free
+      const bool grow = mx > m + kRescale;
+      const bool need = grow && (m > -INFINITY);
+      if (__any_sync(0xffffffffu, need)) {
+        mbar_wait_ab(&bar_pv, (j - 1) & 1, err, &abort_s);
+        tc_fence_after();
+        const float alpha = need ? exp2f(m - mx) : 1.0f;
+#pragma unroll 4
+        for (int c = 0; c < 256; c += 16) {
+          uint32_t v[16];
+          tmem_ld16(tmem + lane_off + 256 + c, v);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+          tmem_st16(tmem + lane_off + 256 + c, v);
+        }
+        tc_fence_before();
+        if (need) l *= alpha;
+      }
+      if (grow) m = mx;
+      const float mref = (m == -INFINITY) ? 0.f : m;
+      uint8_t* pbuf = smem + kPOff + s * 16384;
+      float sum = 0.f;
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float p0 = fast_exp2(x[c8 * 8 + 2 * e] - mref);
+          const float p1 = fast_exp2(x[c8 * 8 + 2 * e + 1] - mref);
+          sum += p0 + p1;
+          w[e] = pack_f16x2(p0, p1);
+        }
+        *reinterpret_cast<uint4*>(pbuf + swz_offset(row, c8, 128)) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      l += sum;
+      fence_async_shared();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_pf[s]);
+    }
+    // ---------------- epilogue
+    if (nch > 0) mbar_wait_ab(&bar_done, 0, err, &abort_s);
+    tc_fence_after();
+    const float sig2 = sink != nullptr ? sink_scale2 * __ldg(sink + row) : -INFINITY;
+    const float M = fmaxf(m, sig2);
+    const float a = (m == -INFINITY) ? 0.f : exp2f(m - M);
+    const float ls = (sig2 == -INFINITY) ? 0.f : exp2f(sig2 - M);
+    const float Z = l * a + ls;
+    const float so = (Z > 0.f && nch > 0) ? (a / Z) * v_scale : 0.f;
+    uint16_t* orow = out + (size_t(t) * 128 + row) * kDv + hf * 256;
+#pragma unroll 2
+    for (int c = 0; c < 256; c += 32) {
+      uint32_t v[32];
+      if (nch > 0) {
+        tmem_ld32(tmem + lane_off + 256 + c, v);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] = 0u;
+      }
+#pragma unroll
+      for (int e = 0; e < 32; e += 8) {
+        uint4 o;
+        o.x = pack_bf16x2(__uint_as_float(v[e + 0]) * so, __uint_as_float(v[e + 1]) * so);
+        o.y = pack_bf16x2(__uint_as_float(v[e + 2]) * so, __uint_as_float(v[e + 3]) * so);
+        o.z = pack_bf16x2(__uint_as_float(v[e + 4]) * so, __uint_as_float(v[e + 5]) * so);
+        o.w = pack_bf16x2(__uint_as_float(v[e + 6]) * so, __uint_as_float(v[e + 7]) * so);
+        *reinterpret_cast<uint4*>(orow + c + e) = o;
+      }
+    }
+    if (hf == 0) {
+      max_logits[size_t(t) * 128 + row] = m_true * kLn2;
+      lse[size_t(t) * 128 + row] = (Z > 0.f) ? (M + log2f(Z)) * kLn2 : -INFINITY;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 512);
 }
+
+}  // namespace
+
+cudaError_t launch_sparse_mla(const MlaArgs& a, cudaStream_t stream, const char** why) {
+  CUtensorMap tm_q128, tm_q64;
+  const uint64_t dims[2] = {uint64_t(kDqk), uint64_t(a.T) * 128};
+  const uint64_t strides[1] = {uint64_t(kDqk)};
+  const uint32_t box128[2] = {128, 128}, box64[2] = {64, 128};
+  if (!encode_tensor_map(&tm_q128, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.q, dims, strides, box128,
+                         CU_TENSOR_MAP_SWIZZLE_128B, why) ||
+      !encode_tensor_map(&tm_q64, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.q, dims, strides, box64,
+                         CU_TENSOR_MAP_SWIZZLE_64B, why))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(mla_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMlaSmem);
+  if (e != cudaSuccess) return e;
+  profile_mark(stream, 0);
+  mla_prefill_kernel<<<a.T * 2, 288, kMlaSmem, stream>>>(
+      tm_q128, tm_q64, a.kv, a.indices, a.topk_length, a.sink, a.c_qk * kLog2e, a.c_sink * kLog2e,
+      a.v_scale, a.T, a.S_kv, a.topk, a.out, a.max_logits, a.lse, a.err);
+  profile_mark(stream, 1);
+  return cudaGetLastError();
+}
+
 }  // namespace msa
