@@ -149,8 +149,8 @@ size_t msa_index_topk_workspace_size(int T, int Hidx, int max_pages);
  * topk_indices: device int32 [Hidx][T][topk] (written in full)
  * workspace:    device, >= msa_index_topk_workspace_size(T, Hidx, max_pages)
  *               bytes, 256-byte aligned; contents on entry are ignored.
- * Supported: D in {64, 128}; 1 <= topk <= 64 (topk >= 2 when blocks must be
- * ranked); Hidx >= 1.
+ * Supported: D in {64, 128}; 1 <= topk <= 64; Hidx a power of two <= 16;
+ * max_pages <= 2048.
  */
 msa_status msa_index_topk(const uint8_t* idx_q, const uint8_t* idx_k_cache,
                           const int32_t* page_table, const int32_t* seq_lens,
