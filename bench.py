@@ -219,13 +219,14 @@ def alg_flops(st, n_keys):
 
 
 def executed_flops(st):
-    """FLOPs the union-tile kernel issues: per 128-row tile (128/G tokens x G
-    heads of one kv head), 128 x 128 x 128 x 4 per block of the tile's union."""
+    """FLOPs the union-tile kernel issues: a CTA holds two 128-row tiles
+    (2 x 128/G tokens x the G heads of one kv head) that walk the union of
+    their rows' selections, 128 x 128 x 128 x 4 per tile per union block."""
     import torch
     w = st["w"]
     cfg = w.cfg
     G = cfg.Hq // cfg.Hkv
-    toks = 128 // G
+    toks = 256 // G
     ids = st["ids"]
     T = w.T
     hpi = cfg.Hq // cfg.Hidx
@@ -243,7 +244,7 @@ def executed_flops(st):
         onehot = torch.zeros((ntile, nblk + 1), dtype=torch.bool, device=s.device)
         onehot.scatter_(1, torch.where(s >= 0, s, nblk), True)
         total += int(onehot[:, :nblk].sum().item())
-    return total * 128.0 * 128 * 128 * 4
+    return total * 2 * 128.0 * 128 * 128 * 4
 
 
 def decode_bytes(st):

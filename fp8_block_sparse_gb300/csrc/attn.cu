@@ -39,16 +39,15 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescale = 8.0f;   // log2 units
 
-// shared memory (byte offsets from a 1024-aligned base)
-constexpr int kQOff = 0;             // 128 rows x 128 e4m3             16 KB
-constexpr int kKOff = 16384;         // 2 stages x 128 keys x 128 e4m3  32 KB
-constexpr int kVOff = 49152;         // 2 stages x V^T f16 image        64 KB
-constexpr int kPOff = 114688;        // 2 buffers x 128 x 128 f16       64 KB
-constexpr int kIdsOff = 180224;      // 128 rows x 64 block ids (int16) 16 KB
-constexpr int kBlistOff = 196608;    // union block list (int16)         4 KB
-constexpr int kBitsOff = 200704;     // union bitmap, 2048 bits         256 B
+// shared memory of the prefill kernel (byte offsets from a 1024-aligned base)
+constexpr int kQOff = 0;             // 2 tiles x 128 rows x 128 e4m3        32 KB
+constexpr int kKOff = 32768;         // 2 stages x 128 keys x 128 e4m3       32 KB
+constexpr int kVOff = 65536;         // 2 stages x V^T f16 image             64 KB
+constexpr int kPOff = 131072;        // 2 tiles x 128 x 128 f16 P            64 KB
+constexpr int kBlistOff = 196608;    // union block list (int16)              4 KB
+constexpr int kBitsOff = 200704;     // union bitmap, 2048 bits              256 B
 constexpr int kPrefillSmem = 200960 + 1024;
-constexpr int kMaxIds = 64;
+constexpr int kPrefillThreads = 384;
 
 constexpr uint32_t kIdescQK = idesc_f32(128, 128);
 constexpr uint32_t kIdescPV = idesc_f32(128, 128);
@@ -91,7 +90,14 @@ vt_convert_kernel(const uint8_t* __restrict__ v_cache, const int32_t* __restrict
 }
 
 // ------------------------------------------------------------ prefill
-__global__ void __launch_bounds__(192, 1)
+// One CTA = two 128-row tiles (X = 0, 1) of one kv head: 2 x 128/G tokens x
+// G heads. Warp roles: 0 producer (TMA), 1 MMA issue, 2-3 idle, 4-7 softmax
+// of tile 0, 8-11 softmax of tile 1 (one thread per row; warp w reads TMEM
+// lanes 32*(w%4)). TMEM: S_0, S_1 at columns 0 and 128, O_0, O_1 at 256 and
+// 384. The MMA issue order per block j is S_0(j+1), S_1(j+1), PV_0(j),
+// PV_1(j), so while one tile's softmax runs the tensor core works on the
+// other tile.
+__global__ void __launch_bounds__(kPrefillThreads, 1)
 attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const uint8_t* __restrict__ vt_img, const int32_t* __restrict__ page_table,
                     const TileInfo* __restrict__ tiles, const int* __restrict__ n_tiles_p,
@@ -103,7 +109,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   __shared__ uint64_t bar_q, bar_kf[2], bar_ke[2], bar_vf[2], bar_ve[2], bar_sf[2], bar_se[2],
-      bar_pf[2], bar_pe[2], bar_pv, bar_done;
+      bar_pf[2], bar_pe[2], bar_done;
   __shared__ uint32_t tmem_base_s;
   __shared__ int n_union_s;
   __shared__ int abort_s;
@@ -114,10 +120,9 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   const int g = blockIdx.x % Hkv;
   const TileInfo ti = tiles[n_tiles - 1 - tile_rank];     // latest (longest) tiles first
   const int G = Hq / Hkv;
-  const int n_tok = min(toks, ti.t_end - ti.t0);
+  const int n_tok = min(2 * toks, ti.t_end - ti.t0);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  int16_t* sIds = reinterpret_cast<int16_t*>(smem + kIdsOff);
   int16_t* sBlist = reinterpret_cast<int16_t*>(smem + kBlistOff);
   uint32_t* sBits = reinterpret_cast<uint32_t*>(smem + kBitsOff);
 
@@ -128,21 +133,22 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bar_kf[s], 1); mbar_init(&bar_ke[s], 1);
       mbar_init(&bar_vf[s], 1); mbar_init(&bar_ve[s], 1);
-      mbar_init(&bar_sf[s], 1); mbar_init(&bar_se[s], 4);
+      mbar_init(&bar_sf[s], 1); mbar_init(&bar_se[s], 4);     // index = tile
       mbar_init(&bar_pf[s], 4); mbar_init(&bar_pe[s], 1);
     }
-    mbar_init(&bar_pv, 1);
     mbar_init(&bar_done, 1);
     fence_barrier_init();
   }
   if (warp == 1) { tmem_alloc(&tmem_base_s, 512); tmem_relinquish(); }
   __syncthreads();
 
-  // ---- each softmax thread owns one row: (token t0 + row/G, head g*G + row%G)
-  const bool is_softmax = warp >= 2;
-  const int row = (warp & 3) * 32 + lane;
-  int n_ids = 0, own = -1, pos = -1, h = 0, t = 0;
+  // ---- softmax threads own rows: row = 128*X + 32*(warp%4) + lane
+  const bool is_softmax = warp >= 4;
+  const int X = (warp >> 2) - 1;
+  const int row = X * 128 + (warp & 3) * 32 + lane;
+  int own = -1, pos = -1, h = 0, t = 0, next_id = -1, ptr = 0;
   bool row_valid = false;
+  const int32_t* src = nullptr;
   if (is_softmax) {
     const int tl = row / G;
     t = ti.t0 + tl;
@@ -151,16 +157,16 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     if (row_valid) {
       pos = ti.p0 + tl;
       own = pos >> 7;
-      const int32_t* src = topk + (size_t(h / (Hq / Hidx)) * T + t) * topk_k;
+      src = topk + (size_t(h / (Hq / Hidx)) * T + t) * topk_k;
       int last = -1;
       for (int k = 0; k < topk_k; ++k) {
         const int id = __ldg(src + k);
         if (id < 0) continue;                                   // -1 padding
         if (id <= last || id > own) { atomicOr(err, MSA_DEVERR_DATA); continue; }
-        sIds[row * kMaxIds + n_ids++] = int16_t(id);
         atomicOr(&sBits[id >> 5], 1u << (id & 31));
         last = id;
       }
+      next_id = topk_k > 0 ? __ldg(src) : -1;
     }
   }
   __syncthreads();
@@ -191,13 +197,15 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   const int nU = n_union_s;
   const uint32_t tmem = tmem_base_s;
 
-  if (warp == 0) {
-    // ---------------- producer: Q once, then K pages (TMA) and V^T images (bulk)
-    if (lane == 0 && nU > 0) {
+  if (warp < 4) {
+    setmaxnreg_dec<56>();
+    if (warp == 0 && lane == 0 && nU > 0) {
+      // ---------------- producer: Q of both tiles, then K pages and V^T images
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
-      mbar_arrive_expect_tx(&bar_q, 16384);
+      mbar_arrive_expect_tx(&bar_q, 32768);
       tma_load_3d(smem + kQOff, &tm_q, &bar_q, 0, g * G, ti.t0);
+      tma_load_3d(smem + kQOff + 16384, &tm_q, &bar_q, 0, g * G, ti.t0 + toks);
       const int32_t* prow = page_table + size_t(ti.b) * max_pages;
       for (int j = 0; j < nU; ++j) {
         const int s = j & 1;
@@ -213,125 +221,149 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         bulk_load(smem + kVOff + s * 32768,
                   vt_img + ((size_t(ti.b) * max_pages + blk) * Hkv + g) * 32768, 32768, &bar_vf[s]);
       }
-    }
-  } else if (warp == 1) {
-    // ---------------- MMA issue: S_{j+1} is issued before PV_j
-    if (lane == 0 && nU > 0 && mbar_wait_ab(&bar_q, 0, err, &abort_s)) {
+    } else if (warp == 1 && lane == 0 && nU > 0 && mbar_wait_ab(&bar_q, 0, err, &abort_s)) {
+      // ---------------- MMA issue
       const uint32_t sq = smem_addr(smem + kQOff);
-      auto issue_s = [&](int j) -> bool {
+      auto issue_s = [&](int j, int x) -> bool {
         const int s = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
-        if (!mbar_wait_ab(&bar_kf[s], ph, err, &abort_s)) return false;
-        if (!mbar_wait_ab(&bar_se[s], ph ^ 1, err, &abort_s)) return false;
+        if (x == 0 && !mbar_wait_ab(&bar_kf[s], (j >> 1) & 1, err, &abort_s)) return false;
+        if (!mbar_wait_ab(&bar_se[x], (j & 1) ^ 1, err, &abort_s)) return false;
         tc_fence_after();
         const uint32_t sk = smem_addr(smem + kKOff + s * 16384);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          mma_e4m3(tmem + s * 128, sdesc_kmajor(sq + 32 * k, 128), sdesc_kmajor(sk + 32 * k, 128),
-                   kIdescQK, k > 0);
-        mma_commit(&bar_ke[s]);
-        mma_commit(&bar_sf[s]);
+          mma_e4m3(tmem + x * 128, sdesc_kmajor(sq + x * 16384 + 32 * k, 128),
+                   sdesc_kmajor(sk + 32 * k, 128), kIdescQK, k > 0);
+        mma_commit(&bar_sf[x]);
+        if (x == 1) mma_commit(&bar_ke[s]);
         return true;
       };
-      bool ok = issue_s(0);
+      bool ok = issue_s(0, 0) && issue_s(0, 1);
       for (int j = 0; ok && j < nU; ++j) {
-        if (j + 1 < nU && !(ok = issue_s(j + 1))) break;
+        if (j + 1 < nU && !(ok = issue_s(j + 1, 0) && issue_s(j + 1, 1))) break;
         const int s = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
-        if (!mbar_wait_ab(&bar_pf[s], ph, err, &abort_s) || !mbar_wait_ab(&bar_vf[s], ph, err, &abort_s)) break;
-        tc_fence_after();
-        const uint32_t sp = smem_addr(smem + kPOff + s * 32768);
+        if (!mbar_wait_ab(&bar_vf[s], (j >> 1) & 1, err, &abort_s)) break;
         const uint32_t sv = smem_addr(smem + kVOff + s * 32768);
+        for (int x = 0; x < 2 && ok; ++x) {
+          if (!(ok = mbar_wait_ab(&bar_pf[x], j & 1, err, &abort_s))) break;
+          tc_fence_after();
+          const uint32_t sp = smem_addr(smem + kPOff + x * 32768);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          mma_f16(tmem + 256, sdesc_kmajor(sp + off, 128), sdesc_kmajor(sv + off, 128), kIdescPV,
-                  (j > 0 || k > 0) ? 1u : 0u);
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+            mma_f16(tmem + 256 + x * 128, sdesc_kmajor(sp + off, 128), sdesc_kmajor(sv + off, 128),
+                    kIdescPV, (j > 0 || k > 0) ? 1u : 0u);
+          }
+          mma_commit(&bar_pe[x]);
         }
+        if (!ok) break;
         mma_commit(&bar_ve[s]);
-        mma_commit(&bar_pe[s]);
-        mma_commit(&bar_pv);
         if (j == nU - 1) mma_commit(&bar_done);
       }
     }
   } else {
-    // ---------------- softmax: one thread per row (TMEM lane `row`)
+    setmaxnreg_inc<224>();
+    // ---------------- softmax of tile X: one thread per row
     const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
-    uint8_t* p_row_base = smem + kPOff;
+    const uint32_t s_col = tmem + lane_off + X * 128;
+    const uint32_t o_col = tmem + lane_off + 256 + X * 128;
+    uint8_t* pbuf = smem + kPOff + X * 32768;
+    const int prow_local = row - X * 128;
+    const uint64_t scale2 = pk2(qk_scale2, qk_scale2);
     float m = -INFINITY, m_true = -INFINITY, l = 0.f;
-    int ptr = 0;
     for (int j = 0; j < nU; ++j) {
-      const int s = j & 1;
-      const uint32_t ph = (j >> 1) & 1;
       const int blk = sBlist[j];
-      const bool sel = ptr < n_ids && sIds[row * kMaxIds + ptr] == blk;
-      ptr += sel ? 1 : 0;
+      const bool sel = row_valid && next_id == blk;
+      if (sel) {
+        ++ptr;
+        next_id = ptr < topk_k ? __ldg(src + ptr) : -1;
+      }
       const int ncol = !sel ? 0 : (blk < own ? 128 : pos - blk * 128 + 1);
-      if (!mbar_wait_ab(&bar_sf[s], ph, err, &abort_s)) break;
+      if (!mbar_wait_ab(&bar_sf[X], j & 1, err, &abort_s)) break;
       tc_fence_after();
       float x[128];
 #pragma unroll
       for (int c = 0; c < 128; c += 32) {
         uint32_t v[32];
-        tmem_ld32(tmem + lane_off + s * 128 + c, v);
+        tmem_ld32(s_col + c, v);
 #pragma unroll
         for (int e = 0; e < 32; ++e) x[c + e] = __uint_as_float(v[e]);
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_se[s]);
+      if (lane == 0) mbar_arrive(&bar_se[X]);
 
-      float mx = -INFINITY;
+      // row max of the raw scores over the valid columns (scale > 0 commutes)
+      float mr = -INFINITY;
+      if (ncol == 128) {
+        float a0 = x[0], a1 = x[1], a2 = x[2], a3 = x[3];
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        x[c] = (c < ncol) ? x[c] * qk_scale2 : -INFINITY;
-        mx = fmaxf(mx, x[c]);
+        for (int c = 4; c < 128; c += 8) {
+          a0 = fmax3(a0, x[c], x[c + 1]);
+          a1 = fmax3(a1, x[c + 2], x[c + 3]);
+          a2 = fmax3(a2, x[c + 4], x[c + 5]);
+          a3 = fmax3(a3, x[c + 6], x[c + 7]);
+        }
+        mr = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
+      } else if (ncol > 0) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c) mr = (c < ncol) ? fmaxf(mr, x[c]) : mr;
       }
+      const float mx = mr * qk_scale2;
       m_true = fmaxf(m_true, mx);
-      // P buffer s is free once PV_{j-2} is done; waiting here first also makes
-      // the pv-barrier parity below unambiguous (at most one PV outstanding)
-      if (!mbar_wait_ab(&bar_pe[s], ph ^ 1, err, &abort_s)) break;
+      // PV of the previous block must be done: it frees P and settles O
+      if (!mbar_wait_ab(&bar_pe[X], (j & 1) ^ 1, err, &abort_s)) break;
       const bool grow = mx > m + kRescale;                    // also when m == -inf
       const bool need_rescale = grow && (m > -INFINITY);
       if (__any_sync(0xffffffffu, need_rescale)) {
-        // O holds PV_0..PV_{j-1}: wait for the last one, then scale this warp's rows
-        if (!mbar_wait_ab(&bar_pv, (j - 1) & 1, err, &abort_s)) break;
         tc_fence_after();
         const float alpha = need_rescale ? exp2f(m - mx) : 1.0f;
 #pragma unroll
         for (int c = 0; c < 128; c += 16) {
           uint32_t v[16];
-          tmem_ld16(tmem + lane_off + 256 + c, v);
+          tmem_ld16(o_col + c, v);
 #pragma unroll
           for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-          tmem_st16(tmem + lane_off + 256 + c, v);
+          tmem_st16(o_col + c, v);
         }
         tc_fence_before();
         if (need_rescale) l *= alpha;
       }
       if (grow) m = mx;
 
-      // P row (f16) into the swizzled A operand of buffer s
-      const float mref = (m == -INFINITY) ? 0.f : m;
-      uint8_t* pbuf = p_row_base + s * 32768;
-      float sum = 0.f;
+      // P = exp2(S * scale - m) in f16, into the swizzled A operand of tile X
+      if (ncol == 0) {
 #pragma unroll
-      for (int c8 = 0; c8 < 16; ++c8) {
-        uint32_t w[4];
+        for (int c8 = 0; c8 < 16; ++c8)
+          *reinterpret_cast<uint4*>(pbuf + (c8 >> 3) * 16384 + swz_offset(prow_local, c8 & 7, 128)) =
+              make_uint4(0u, 0u, 0u, 0u);
+      } else {
+        const uint64_t negm = pk2(-m, -m);
+        uint64_t acc = pk2(0.f, 0.f);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float p0 = fast_exp2(x[c8 * 8 + 2 * e] - mref);
-          const float p1 = fast_exp2(x[c8 * 8 + 2 * e + 1] - mref);
-          sum += p0 + p1;
-          w[e] = pack_f16x2(p0, p1);
+        for (int c8 = 0; c8 < 16; ++c8) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = c8 * 8 + 2 * e;
+            const float2 y = unpk2(ffma2(pk2(x[c], x[c + 1]), scale2, negm));
+            float p0 = fast_exp2(y.x), p1 = fast_exp2(y.y);
+            if (ncol < 128) {
+              p0 = c < ncol ? p0 : 0.f;
+              p1 = c + 1 < ncol ? p1 : 0.f;
+            }
+            acc = fadd2(acc, pk2(p0, p1));
+            w[e] = pack_f16x2(p0, p1);
+          }
+          *reinterpret_cast<uint4*>(pbuf + (c8 >> 3) * 16384 + swz_offset(prow_local, c8 & 7, 128)) =
+              make_uint4(w[0], w[1], w[2], w[3]);
         }
-        *reinterpret_cast<uint4*>(pbuf + (c8 >> 3) * 16384 + swz_offset(row, c8 & 7, 128)) =
-            make_uint4(w[0], w[1], w[2], w[3]);
+        const float2 a2 = unpk2(acc);
+        l += a2.x + a2.y;
       }
-      l += sum;
       fence_async_shared();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_pf[s]);
+      if (lane == 0) mbar_arrive(&bar_pf[X]);
     }
 
     // ---------------- epilogue: O / (l + sink), lse, max_logit
@@ -348,7 +380,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     for (int c = 0; c < 128; c += 32) {
       uint32_t v[32];
       if (nU > 0) {
-        tmem_ld32(tmem + lane_off + 256 + c, v);
+        tmem_ld32(o_col + c, v);
       } else {
 #pragma unroll
         for (int e = 0; e < 32; ++e) v[e] = 0u;             // no block: O = 0
@@ -374,7 +406,6 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   __syncthreads();
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
-
 
 // ------------------------------------------------------------ paged decode
 // One CTA per (query token, kv head, chunk): the G q heads of the kv head
@@ -833,17 +864,17 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream, const cha
                            CU_TENSOR_MAP_SWIZZLE_128B, why))
       return cudaErrorInvalidValue;
   }
-  plan_tiles_kernel<<<1, 256, 0, stream>>>(a.seq_lens, a.cu_q, a.B, toks, a.max_pages, max_tiles,
-                                           tiles, n_tiles, a.err);
+  plan_tiles_kernel<<<1, 256, 0, stream>>>(a.seq_lens, a.cu_q, a.B, 2 * toks, a.max_pages,
+                                           max_tiles, tiles, n_tiles, a.err);
   vt_convert_kernel<<<dim3(a.max_pages, a.B, a.Hkv), 256, 0, stream>>>(
       a.v_cache, a.page_table, a.seq_lens, a.Hkv, a.max_pages, a.num_pages, ws, a.err);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(attn_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrefillSmem);
   if (e != cudaSuccess) return e;
-  const int grid = ((a.T + toks - 1) / toks + a.B) * a.Hkv;
+  const int grid = ((a.T + 2 * toks - 1) / (2 * toks) + a.B) * a.Hkv;
   profile_mark(stream, 0);
-  attn_prefill_kernel<<<grid, 192, kPrefillSmem, stream>>>(
+  attn_prefill_kernel<<<grid, kPrefillThreads, kPrefillSmem, stream>>>(
       tm_q, tm_k, ws, a.page_table, tiles, n_tiles, a.topk, a.sink, a.c_qk * kLog2e,
       a.c_sink * kLog2e, a.v_scale, a.T, a.Hq, a.Hkv, a.Hidx, toks, a.topk_k, a.max_pages,
       a.num_pages, a.out, a.max_logit, a.lse, a.err);
