@@ -10,7 +10,7 @@
 
 #include <cudaTypedefs.h>
 
-#include "../../include/msa.h"
+#include "msa.h"
 #include "internal.h"
 
 namespace msa {

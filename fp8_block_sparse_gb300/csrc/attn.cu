@@ -40,13 +40,13 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescale = 8.0f;   // log2 units
 
 // shared memory of the prefill kernel (byte offsets from a 1024-aligned base)
+constexpr int kStages = 3;
 constexpr int kQOff = 0;             // 2 tiles x 128 rows x 128 e4m3        32 KB
-constexpr int kKOff = 32768;         // 2 stages x 128 keys x 128 e4m3       32 KB
-constexpr int kVOff = 65536;         // 2 stages x V^T f16 image             64 KB
-constexpr int kPOff = 131072;        // 2 tiles x 128 x 128 f16 P            64 KB
-constexpr int kBlistOff = 196608;    // union block list (int16)              4 KB
-constexpr int kBitsOff = 200704;     // union bitmap, 2048 bits              256 B
-constexpr int kPrefillSmem = 200960 + 1024;
+constexpr int kKOff = 32768;         // 3 stages x 128 keys x 128 e4m3       48 KB
+constexpr int kVOff = 81920;         // 3 stages x V^T f16 image             96 KB
+constexpr int kBlistOff = 180224;    // union block list (int16)              4 KB
+constexpr int kBitsOff = 184320;     // union bitmap, 2048 bits              256 B
+constexpr int kPrefillSmem = 184576 + 1024;
 constexpr int kPrefillThreads = 384;
 
 constexpr uint32_t kIdescQK = idesc_f32(128, 128);
@@ -93,10 +93,16 @@ vt_convert_kernel(const uint8_t* __restrict__ v_cache, const int32_t* __restrict
 // One CTA = two 128-row tiles (X = 0, 1) of one kv head: 2 x 128/G tokens x
 // G heads. Warp roles: 0 producer (TMA), 1 MMA issue, 2-3 idle, 4-7 softmax
 // of tile 0, 8-11 softmax of tile 1 (one thread per row; warp w reads TMEM
-// lanes 32*(w%4)). TMEM: S_0, S_1 at columns 0 and 128, O_0, O_1 at 256 and
-// 384. The MMA issue order per block j is S_0(j+1), S_1(j+1), PV_0(j),
-// PV_1(j), so while one tile's softmax runs the tensor core works on the
-// other tile.
+// lanes 32*(w%4)). TMEM: S_0 and S_1 at columns 0 and 128, O_0 and O_1 at 256
+// and 384. P (f16, two per 32-bit column) overwrites the first 64 columns of
+// its tile's S once the softmax has read S, and the PV MMA takes it as the A
+// operand straight from TMEM, so P never touches shared memory (which would
+// otherwise bound the kernel: a 128x128 f16 MMA with both operands in smem
+// reads 128 B/clk). Per block j the MMA issue order is PV_0(j), S_0(j+1),
+// PV_1(j), S_1(j+1); tcgen05 MMAs of one thread run in order, so S_X(j+1)
+// overwrites P_X(j) only after PV_X(j) has read it, and the commit of S_X(j+1)
+// also proves PV_X(j) complete -- the softmax needs no other barrier before
+// touching O or writing the next P.
 __global__ void __launch_bounds__(kPrefillThreads, 1)
 attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const uint8_t* __restrict__ vt_img, const int32_t* __restrict__ page_table,
@@ -108,8 +114,8 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     float* __restrict__ lse, unsigned* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  __shared__ uint64_t bar_q, bar_kf[2], bar_ke[2], bar_vf[2], bar_ve[2], bar_sf[2], bar_se[2],
-      bar_pf[2], bar_pe[2], bar_done;
+  __shared__ uint64_t bar_q, bar_kf[kStages], bar_ke[kStages], bar_vf[kStages], bar_ve[kStages],
+      bar_sf[2], bar_pf[2], bar_done;
   __shared__ uint32_t tmem_base_s;
   __shared__ int n_union_s;
   __shared__ int abort_s;
@@ -130,12 +136,11 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   if (tid == 0) {
     abort_s = 0;
     mbar_init(&bar_q, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(&bar_kf[s], 1); mbar_init(&bar_ke[s], 1);
       mbar_init(&bar_vf[s], 1); mbar_init(&bar_ve[s], 1);
-      mbar_init(&bar_sf[s], 1); mbar_init(&bar_se[s], 4);     // index = tile
-      mbar_init(&bar_pf[s], 4); mbar_init(&bar_pe[s], 1);
     }
+    for (int x = 0; x < 2; ++x) { mbar_init(&bar_sf[x], 1); mbar_init(&bar_pf[x], 4); }
     mbar_init(&bar_done, 1);
     fence_barrier_init();
   }
@@ -208,8 +213,8 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       tma_load_3d(smem + kQOff + 16384, &tm_q, &bar_q, 0, g * G, ti.t0 + toks);
       const int32_t* prow = page_table + size_t(ti.b) * max_pages;
       for (int j = 0; j < nU; ++j) {
-        const int s = j & 1;
-        const uint32_t ph = ((j >> 1) & 1) ^ 1;
+        const int s = j % kStages;
+        const uint32_t ph = ((j / kStages) & 1) ^ 1;
         const int blk = sBlist[j];
         int page = __ldg(prow + blk);
         if (page < 0 || page >= num_pages) { atomicOr(err, MSA_DEVERR_DATA); page = 0; }
@@ -225,9 +230,8 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       // ---------------- MMA issue
       const uint32_t sq = smem_addr(smem + kQOff);
       auto issue_s = [&](int j, int x) -> bool {
-        const int s = j & 1;
-        if (x == 0 && !mbar_wait_ab(&bar_kf[s], (j >> 1) & 1, err, &abort_s)) return false;
-        if (!mbar_wait_ab(&bar_se[x], (j & 1) ^ 1, err, &abort_s)) return false;
+        const int s = j % kStages;
+        if (x == 0 && !mbar_wait_ab(&bar_kf[s], (j / kStages) & 1, err, &abort_s)) return false;
         tc_fence_after();
         const uint32_t sk = smem_addr(smem + kKOff + s * 16384);
 #pragma unroll
@@ -240,25 +244,21 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       };
       bool ok = issue_s(0, 0) && issue_s(0, 1);
       for (int j = 0; ok && j < nU; ++j) {
-        if (j + 1 < nU && !(ok = issue_s(j + 1, 0) && issue_s(j + 1, 1))) break;
-        const int s = j & 1;
-        if (!mbar_wait_ab(&bar_vf[s], (j >> 1) & 1, err, &abort_s)) break;
+        const int s = j % kStages;
+        if (!mbar_wait_ab(&bar_vf[s], (j / kStages) & 1, err, &abort_s)) break;
         const uint32_t sv = smem_addr(smem + kVOff + s * 32768);
-        for (int x = 0; x < 2 && ok; ++x) {
+        for (int x = 0; x < 2; ++x) {
           if (!(ok = mbar_wait_ab(&bar_pf[x], j & 1, err, &abort_s))) break;
           tc_fence_after();
-          const uint32_t sp = smem_addr(smem + kPOff + x * 32768);
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-            mma_f16(tmem + 256 + x * 128, sdesc_kmajor(sp + off, 128), sdesc_kmajor(sv + off, 128),
-                    kIdescPV, (j > 0 || k > 0) ? 1u : 0u);
-          }
-          mma_commit(&bar_pe[x]);
+          for (int k = 0; k < 8; ++k)
+            mma_f16_ts(tmem + 256 + x * 128, tmem + x * 128 + 8 * k,
+                       sdesc_kmajor(sv + (k >> 2) * 16384 + (k & 3) * 32, 128), kIdescPV,
+                       (j > 0 || k > 0) ? 1u : 0u);
+          if (x == 1) mma_commit(&bar_ve[s]);
+          if (j + 1 < nU && !(ok = issue_s(j + 1, x))) break;
         }
-        if (!ok) break;
-        mma_commit(&bar_ve[s]);
-        if (j == nU - 1) mma_commit(&bar_done);
+        if (ok && j == nU - 1) mma_commit(&bar_done);
       }
     }
   } else {
@@ -267,8 +267,6 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
     const uint32_t s_col = tmem + lane_off + X * 128;
     const uint32_t o_col = tmem + lane_off + 256 + X * 128;
-    uint8_t* pbuf = smem + kPOff + X * 32768;
-    const int prow_local = row - X * 128;
     const uint64_t scale2 = pk2(qk_scale2, qk_scale2);
     float m = -INFINITY, m_true = -INFINITY, l = 0.f;
     for (int j = 0; j < nU; ++j) {
@@ -279,20 +277,16 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         next_id = ptr < topk_k ? __ldg(src + ptr) : -1;
       }
       const int ncol = !sel ? 0 : (blk < own ? 128 : pos - blk * 128 + 1);
+      // S_X(j) done (and with it PV_X(j-1): O is settled and P may be rewritten)
       if (!mbar_wait_ab(&bar_sf[X], j & 1, err, &abort_s)) break;
       tc_fence_after();
       float x[128];
+      {
+        uint32_t v[128];
+        tmem_ld128(s_col, v);
 #pragma unroll
-      for (int c = 0; c < 128; c += 32) {
-        uint32_t v[32];
-        tmem_ld32(s_col + c, v);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) x[c + e] = __uint_as_float(v[e]);
+        for (int e = 0; e < 128; ++e) x[e] = __uint_as_float(v[e]);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_se[X]);
-
       // row max of the raw scores over the valid columns (scale > 0 commutes)
       float mr = -INFINITY;
       if (ncol == 128) {
@@ -311,12 +305,9 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       }
       const float mx = mr * qk_scale2;
       m_true = fmaxf(m_true, mx);
-      // PV of the previous block must be done: it frees P and settles O
-      if (!mbar_wait_ab(&bar_pe[X], (j & 1) ^ 1, err, &abort_s)) break;
       const bool grow = mx > m + kRescale;                    // also when m == -inf
       const bool need_rescale = grow && (m > -INFINITY);
       if (__any_sync(0xffffffffu, need_rescale)) {
-        tc_fence_after();
         const float alpha = need_rescale ? exp2f(m - mx) : 1.0f;
 #pragma unroll
         for (int c = 0; c < 128; c += 16) {
@@ -326,42 +317,41 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
           tmem_st16(o_col + c, v);
         }
-        tc_fence_before();
         if (need_rescale) l *= alpha;
       }
       if (grow) m = mx;
 
-      // P = exp2(S * scale - m) in f16, into the swizzled A operand of tile X
-      if (ncol == 0) {
-#pragma unroll
-        for (int c8 = 0; c8 < 16; ++c8)
-          *reinterpret_cast<uint4*>(pbuf + (c8 >> 3) * 16384 + swz_offset(prow_local, c8 & 7, 128)) =
-              make_uint4(0u, 0u, 0u, 0u);
-      } else {
+      // P = exp2(S * scale - m) as f16 pairs over the first 64 columns of S_X.
+      // Three explicit paths so the common full block carries no masking.
+      uint32_t w[64];
+      if (ncol == 128) {
         const uint64_t negm = pk2(-m, -m);
-        uint64_t acc = pk2(0.f, 0.f);
+        uint64_t acc0 = pk2(0.f, 0.f), acc1 = acc0;
 #pragma unroll
-        for (int c8 = 0; c8 < 16; ++c8) {
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c = c8 * 8 + 2 * e;
-            const float2 y = unpk2(ffma2(pk2(x[c], x[c + 1]), scale2, negm));
-            float p0 = fast_exp2(y.x), p1 = fast_exp2(y.y);
-            if (ncol < 128) {
-              p0 = c < ncol ? p0 : 0.f;
-              p1 = c + 1 < ncol ? p1 : 0.f;
-            }
-            acc = fadd2(acc, pk2(p0, p1));
-            w[e] = pack_f16x2(p0, p1);
-          }
-          *reinterpret_cast<uint4*>(pbuf + (c8 >> 3) * 16384 + swz_offset(prow_local, c8 & 7, 128)) =
-              make_uint4(w[0], w[1], w[2], w[3]);
+        for (int c = 0; c < 128; c += 2) {
+          const float2 y = unpk2(ffma2(pk2(x[c], x[c + 1]), scale2, negm));
+          const float p0 = fast_exp2(y.x), p1 = fast_exp2(y.y);
+          if (c & 2) acc1 = fadd2(acc1, pk2(p0, p1)); else acc0 = fadd2(acc0, pk2(p0, p1));
+          w[c >> 1] = pack_f16x2(p0, p1);
         }
-        const float2 a2 = unpk2(acc);
+        const float2 a2 = unpk2(fadd2(acc0, acc1));
         l += a2.x + a2.y;
+      } else if (ncol > 0) {
+        float sum = 0.f;
+#pragma unroll
+        for (int c = 0; c < 128; c += 2) {
+          const float p0 = c < ncol ? fast_exp2(fmaf(x[c], qk_scale2, -m)) : 0.f;
+          const float p1 = c + 1 < ncol ? fast_exp2(fmaf(x[c + 1], qk_scale2, -m)) : 0.f;
+          sum += p0 + p1;
+          w[c >> 1] = pack_f16x2(p0, p1);
+        }
+        l += sum;
+      } else {
+#pragma unroll
+        for (int c = 0; c < 64; ++c) w[c] = 0u;
       }
-      fence_async_shared();
+      tmem_st64(s_col, w);
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_pf[X]);
     }

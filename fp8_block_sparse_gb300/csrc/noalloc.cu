@@ -24,7 +24,7 @@
 #include <mutex>
 #include <string>
 
-#include "../../include/msa.h"
+#include "msa.h"
 #include "internal.h"
 
 namespace msa {
