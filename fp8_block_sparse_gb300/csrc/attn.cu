@@ -401,31 +401,42 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 // One CTA per (query token, kv head, chunk): the G q heads of the kv head
 // share one walk over the ascending union of their index heads' selections;
 // the union is cut into at most kDecMaxChunks balanced chunks (flash-decoding
-// split) so that enough CTAs stream pages at once. Per block:
-//   S^T = K Q^T   tcgen05 e4m3, M = 128 keys (the page straight from TMA),
-//                 N = 16 query columns (G used), K = 128;
-//   P             softmax across TMEM lanes: one thread per key, the row max
-//                 of a block combined over the four softmax warps through
-//                 shared memory (one named barrier per block); every thread
-//                 keeps identical copies of the running max of each row and
-//                 its own partial row sums (summed once at the end);
-//   O^T += V^T P^T  tcgen05 f16, A = the page's V^T f16 image written by four
-//                 converter warps, B = P (16 rows x 128 keys, f16).
-// A chunk leaves its unnormalised O, running max, row sum and true max in the
-// workspace; decode_combine_kernel merges the chunks and applies the sink.
+// split) so that enough CTAs stream pages at once. Decode is bound by HBM
+// (every selected K and V page is read once per (token, kv head)), so the
+// kernel spends no work reshaping pages: per 128-key block
+//   S^T = K Q^T       tcgen05 e4m3, A = the K page from TMA (M = 128 keys),
+//                     B = the G query rows (N = 16), K = 128;
+//   P                 softmax across TMEM lanes, one thread per key. The row
+//                     max is lazy: a block only costs one vote and one barrier
+//                     unless some score exceeds the running reference by
+//                     2^8, when that row's exact block max is reduced;
+//   O^T += V^T P^T    tcgen05 e4m3 three times, A = the V page straight from
+//                     TMA read as an MN-major operand, B = P split into three
+//                     e4m3 terms (P rounded, then the rounded remainder, then
+//                     the remainder of that): together they carry P to about
+//                     2^-12, where e4m3 P alone would cost ~2.5% and two terms
+//                     ~0.4%. P is taken relative to a reference 4 below the
+//                     running max (so the key that set it has P = 16 and no P
+//                     exceeds 2^8 < 448), which keeps the remainders of the
+//                     large terms clear of e4m3's subnormal range.
+// A chunk leaves its unnormalised O, reference max, row sum and true max in
+// the workspace; decode_combine_kernel merges the chunks and applies the sink.
 constexpr int kDecChunk = 32;
-constexpr int kDecStages = 3;
+constexpr int kDecKStages = 3;
+constexpr int kDecVStages = 2;
 constexpr int kDecMaxList = 1024;   // union entries kept (<= 16 index heads x 64)
-constexpr int kDKOff = 0;            // kDecStages x 16 KB K pages
-constexpr int kDVOff = 49152;        // kDecStages x 16 KB V pages (row-major, unswizzled)
-constexpr int kDVTOff = 98304;       // 2 x 32 KB V^T f16 images
-constexpr int kDPOff = 163840;       // 2 x 4 KB P (16 rows x 128 keys f16)
-constexpr int kDQOff = 172032;       // 16 rows x 128 e4m3
-constexpr int kDListOff = 174080;    // union list (int16)
-constexpr int kDMaskOff = 176128;    // per-entry row mask (uint16)
-constexpr int kDBitsOff = 178176;    // 16 bitmaps x 2048 bits
-constexpr int kDecodeSmem = 178176 + 16 * 256 + 1024;
+constexpr int kDKOff = 0;           // kDecKStages x 16 KB K pages (SW128)
+constexpr int kDVOff = 49152;       // kDecVStages x 16 KB V pages (SW128)
+constexpr int kDPOff = 81920;       // 2 x 3 terms x 2 KB: 16 rows x 128 keys e4m3 (SW128)
+constexpr int kDBitsOff = 81920;    // setup only: 16 bitmaps x 2048 bits (aliases P)
+constexpr int kDQOff = 94208;       // 16 rows x 128 e4m3
+constexpr int kDListOff = 96256;    // union list (int16)
+constexpr int kDMaskOff = 98304;    // per-entry row mask (uint16)
+constexpr int kDecodeSmem = 100352 + 1024;
+constexpr float kDecLimit = 8.0f;   // log2 of the largest P before the reference moves
+constexpr float kDecHead = 4.0f;    // log2 of P at the key that set the reference
 constexpr uint32_t kIdescDec = idesc_f32(128, 16);
+constexpr uint32_t kIdescDecT = idesc_f32(128, 16) | (1u << 15);   // A MN-major
 
 struct DecodePartial {   // per (token, kv head, chunk, row)
   float m, l, m_true, pad;
@@ -436,7 +447,7 @@ __host__ __device__ inline int dec_max_chunks(int n_idx_per_group, int topk, int
   return max(1, (cap + kDecChunk - 1) / kDecChunk);
 }
 
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(192, 2)
 attn_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const int32_t* __restrict__ page_table,
                    const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ cu_q,
@@ -446,13 +457,13 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                    int* __restrict__ n_chunks_out, unsigned* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  __shared__ uint64_t bar_q, bar_kvf[kDecStages], bar_kve[kDecStages], bar_sf[2], bar_se[2],
-      bar_pf[2], bar_pe[2], bar_vtf[2], bar_vte[2], bar_pv, bar_done;
+  __shared__ uint64_t bar_q, bar_kf[kDecKStages], bar_ke[kDecKStages], bar_vf[kDecVStages],
+      bar_ve[kDecVStages], bar_sf[2], bar_se[2], bar_pf[2], bar_pe[2], bar_pv, bar_done, bar_vt;
   __shared__ uint32_t tmem_base_s;
   __shared__ int n_union_s;
-  __shared__ float red[2][4][16];
-  __shared__ float lsum[4][16];
   __shared__ int abort_s;
+  __shared__ uint32_t flags[2][4];
+  __shared__ float red[2][4][16];
 
   const int G = Hq / Hkv;
   const int c = blockIdx.x % max_chunks;
@@ -476,9 +487,9 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
   int16_t* sList = reinterpret_cast<int16_t*>(smem + kDListOff);
   uint16_t* sMask = reinterpret_cast<uint16_t*>(smem + kDMaskOff);
   uint32_t* sBits = reinterpret_cast<uint32_t*>(smem + kDBitsOff);
-  for (int x = tid; x < n_idx * 64; x += 320) sBits[x] = 0u;
+  for (int x = tid; x < n_idx * 64; x += 192) sBits[x] = 0u;
   __syncthreads();
-  for (int x = tid; x < n_idx * topk_k; x += 320) {
+  for (int x = tid; x < n_idx * topk_k; x += 192) {
     const int il = x / topk_k;
     const int id = __ldg(topk + (size_t(i_first + il) * T + t) * topk_k + (x - il * topk_k));
     if (id < 0) continue;
@@ -519,7 +530,7 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     }
     if (lane == 0) n_union_s = min(base, kDecMaxList);
   }
-  __syncthreads();
+  __syncthreads();                                   // the bitmaps (over P) are dead now
   const int nU = n_union_s;
   const int nch = min(max_chunks, (nU + kDecChunk - 1) / kDecChunk);
   if (c == 0 && tid == 0) n_chunks_out[unit] = nch;
@@ -530,14 +541,15 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
   if (tid == 0) {
     abort_s = 0;
     mbar_init(&bar_q, 1);
-    for (int s = 0; s < kDecStages; ++s) { mbar_init(&bar_kvf[s], 1); mbar_init(&bar_kve[s], 5); }
+    for (int s = 0; s < kDecKStages; ++s) { mbar_init(&bar_kf[s], 1); mbar_init(&bar_ke[s], 1); }
+    for (int s = 0; s < kDecVStages; ++s) { mbar_init(&bar_vf[s], 1); mbar_init(&bar_ve[s], 1); }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bar_sf[s], 1); mbar_init(&bar_se[s], 4);
       mbar_init(&bar_pf[s], 4); mbar_init(&bar_pe[s], 1);
-      mbar_init(&bar_vtf[s], 4); mbar_init(&bar_vte[s], 1);
     }
     mbar_init(&bar_pv, 1);
     mbar_init(&bar_done, 1);
+    mbar_init(&bar_vt, 1);
     fence_barrier_init();
   }
   if (warp == 1) { tmem_alloc(&tmem_base_s, 64); tmem_relinquish(); }
@@ -546,27 +558,59 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
   const uint32_t tmem = tmem_base_s;          // S^T buffers at cols 0, 16; O^T at 32
 
   if (warp == 0) {
+    // Producer. Rows of the last page past seq_len hold whatever the cache
+    // pool holds there (possibly e4m3 NaN); PV would turn 0 * NaN into NaN,
+    // so that page's V is landed on its own barrier, its tail rows are
+    // zeroed by the warp, and only then is it handed to the MMA.
     if (lane == 0) {
       mbar_arrive_expect_tx(&bar_q, 16 * 128);
       tma_load_2d(smem + kDQOff, &tm_q, &bar_q, 0, t * Hq + g * G);
-      const int32_t* prow = page_table + size_t(b) * max_pages;
-      for (int jj = 0; jj < n; ++jj) {
-        const int s = jj % kDecStages;
-        if (!mbar_wait_ab(&bar_kve[s], ((jj / kDecStages) & 1) ^ 1, err, &abort_s)) break;
-        int page = __ldg(prow + sList[j0 + jj]);
-        if (page < 0 || page >= num_pages) { atomicOr(err, MSA_DEVERR_DATA); page = 0; }
-        const int row0 = (page * Hkv + g) * 128;
-        mbar_arrive_expect_tx(&bar_kvf[s], 32768);
-        tma_load_2d(smem + kDKOff + s * 16384, &tm_k, &bar_kvf[s], 0, row0);
-        tma_load_2d(smem + kDVOff + s * 16384, &tm_v, &bar_kvf[s], 0, row0);
+    }
+    const int32_t* prow = page_table + size_t(b) * max_pages;
+    const int tail_blk = (L - 1) >> 7, tail_rows = L - tail_blk * 128;
+    for (int jj = 0; jj < n; ++jj) {
+      const int s = jj % kDecKStages, sv = jj % kDecVStages;
+      const uint32_t ph = ((jj / kDecKStages) & 1) ^ 1, phv = ((jj / kDecVStages) & 1) ^ 1;
+      const int blk = sList[j0 + jj];
+      int page = __ldg(prow + blk);
+      if (page < 0 || page >= num_pages) {
+        if (lane == 0) atomicOr(err, MSA_DEVERR_DATA);
+        page = 0;
+      }
+      const int row0 = (page * Hkv + g) * 128;
+      uint8_t* vs = smem + kDVOff + sv * 16384;
+      int ok = 1;
+      if (lane == 0) {
+        ok = mbar_wait_ab(&bar_ke[s], ph, err, &abort_s);
+        if (ok) {
+          mbar_arrive_expect_tx(&bar_kf[s], 16384);
+          tma_load_2d(smem + kDKOff + s * 16384, &tm_k, &bar_kf[s], 0, row0);
+          ok = mbar_wait_ab(&bar_ve[sv], phv, err, &abort_s);
+        }
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      if (blk == tail_blk && tail_rows < 128) {   // at most once per CTA
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bar_vt, 16384);
+          tma_load_2d(vs, &tm_v, &bar_vt, 0, row0);
+        }
+        if (!mbar_wait_ab(&bar_vt, 0, err, &abort_s)) break;
+        uint4* rows = reinterpret_cast<uint4*>(vs + tail_rows * 128);   // swizzle stays inside a row
+        for (int x = lane; x < (128 - tail_rows) * 8; x += 32) rows[x] = make_uint4(0u, 0u, 0u, 0u);
+        fence_async_shared();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_vf[sv]);
+      } else if (lane == 0) {
+        mbar_arrive_expect_tx(&bar_vf[sv], 16384);
+        tma_load_2d(vs, &tm_v, &bar_vf[sv], 0, row0);
       }
     }
   } else if (warp == 1) {
     if (lane == 0 && mbar_wait_ab(&bar_q, 0, err, &abort_s)) {
       const uint32_t sq = smem_addr(smem + kDQOff);
       auto issue_s = [&](int jj) -> bool {
-        const int s = jj % kDecStages, sb = jj & 1;
-        if (!mbar_wait_ab(&bar_kvf[s], (jj / kDecStages) & 1, err, &abort_s)) return false;
+        const int s = jj % kDecKStages, sb = jj & 1;
+        if (!mbar_wait_ab(&bar_kf[s], (jj / kDecKStages) & 1, err, &abort_s)) return false;
         if (!mbar_wait_ab(&bar_se[sb], ((jj >> 1) & 1) ^ 1, err, &abort_s)) return false;
         tc_fence_after();
         const uint32_t sk = smem_addr(smem + kDKOff + s * 16384);
@@ -574,58 +618,32 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         for (int k = 0; k < 4; ++k)
           mma_e4m3(tmem + sb * 16, sdesc_kmajor(sk + 32 * k, 128), sdesc_kmajor(sq + 32 * k, 128),
                    kIdescDec, k > 0);
-        mma_commit(&bar_kve[s]);
+        mma_commit(&bar_ke[s]);
         mma_commit(&bar_sf[sb]);
         return true;
       };
       bool ok = n > 0 && issue_s(0);
       for (int jj = 0; ok && jj < n; ++jj) {
         if (jj + 1 < n && !(ok = issue_s(jj + 1))) break;
-        const int sb = jj & 1;
-        const uint32_t ph = (jj >> 1) & 1;
-        if (!mbar_wait_ab(&bar_pf[sb], ph, err, &abort_s) || !mbar_wait_ab(&bar_vtf[sb], ph, err, &abort_s)) break;
+        const int s = jj % kDecVStages, sb = jj & 1;
+        if (!mbar_wait_ab(&bar_pf[sb], (jj >> 1) & 1, err, &abort_s) ||
+            !mbar_wait_ab(&bar_vf[s], (jj / kDecVStages) & 1, err, &abort_s))
+          break;
         tc_fence_after();
-        const uint32_t svt = smem_addr(smem + kDVTOff + sb * 32768);
-        const uint32_t sp = smem_addr(smem + kDPOff + sb * 4096);
+        const uint32_t sv = smem_addr(smem + kDVOff + s * 16384);
+        const uint32_t sp = smem_addr(smem + kDPOff + sb * 6144);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          mma_f16(tmem + 32, sdesc_kmajor(svt + (k >> 2) * 16384 + (k & 3) * 32, 128),
-                  sdesc_kmajor(sp + (k >> 2) * 2048 + (k & 3) * 32, 128), kIdescDec,
-                  (jj > 0 || k > 0) ? 1u : 0u);
-        }
-        mma_commit(&bar_vte[sb]);
+        for (int part = 0; part < 3; ++part)          // the three terms of P
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_e4m3(tmem + 32, sdesc_kmajor(sv + 4096 * k, 128),
+                     sdesc_kmajor(sp + part * 2048 + 32 * k, 128), kIdescDecT,
+                     (jj > 0 || part > 0 || k > 0) ? 1u : 0u);
+        mma_commit(&bar_ve[s]);
         mma_commit(&bar_pe[sb]);
         mma_commit(&bar_pv);
         if (jj == n - 1) mma_commit(&bar_done);
       }
-    }
-  } else if (warp >= 6) {
-    // ---------------- converters: V page (e4m3, [key][d]) -> V^T f16 image
-    const int ct = tid - 192;
-    for (int jj = 0; jj < n; ++jj) {
-      const int s = jj % kDecStages, sb = jj & 1;
-      if (!mbar_wait_ab(&bar_kvf[s], (jj / kDecStages) & 1, err, &abort_s)) break;
-      if (!mbar_wait_ab(&bar_vte[sb], ((jj >> 1) & 1) ^ 1, err, &abort_s)) break;
-      const uint8_t* vt = smem + kDVOff + s * 16384;
-      uint8_t* dst = smem + kDVTOff + sb * 32768;
-      const int nvalid = min(128, pos + 1 - int(sList[j0 + jj]) * 128);
-#pragma unroll 4
-      for (int x = ct; x < 2048; x += 128) {
-        const int d = x & 127, cc = (x >> 7) & 7, a = x >> 10;
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int k0 = a * 64 + cc * 8 + 2 * e;
-          const uint32_t lo = k0 < nvalid ? vt[k0 * 128 + d] : 0u;
-          const uint32_t hi = k0 + 1 < nvalid ? vt[(k0 + 1) * 128 + d] : 0u;
-          w[e] = e4m3x2_to_f16x2(uint16_t(lo | (hi << 8)));
-        }
-        *reinterpret_cast<uint4*>(dst + a * 16384 + swz_offset(d, cc, 128)) =
-            make_uint4(w[0], w[1], w[2], w[3]);
-      }
-      fence_async_shared();
-      __syncwarp();
-      if (lane == 0) { mbar_arrive(&bar_vtf[sb]); mbar_arrive(&bar_kve[s]); }
     }
   } else {
     // ---------------- softmax: thread = key lane of S^T and d lane of O^T
@@ -649,30 +667,43 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_se[sb]);
       float x[16];
+      uint32_t over = 0;
 #pragma unroll
       for (int r = 0; r < 16; ++r) {
         x[r] = (r < G && kvalid && ((rmask >> r) & 1u)) ? __uint_as_float(v[r]) * qk_scale2 : -INFINITY;
-        float mr = x[r];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mr = fmaxf(mr, __shfl_xor_sync(0xffffffffu, mr, o));
-        if (lane == 0) red[sb][q4][r] = mr;
+        mt[r] = fmaxf(mt[r], x[r]);
+        over |= (x[r] > m[r] + kDecLimit) ? (1u << r) : 0u;
       }
+      over = __reduce_or_sync(0xffffffffu, over);
+      if (lane == 0) flags[sb][q4] = over;
       asm volatile("bar.sync 1, 128;" ::: "memory");
+      const uint32_t E = flags[sb][0] | flags[sb][1] | flags[sb][2] | flags[sb][3];
       float alpha[16];
       bool need = false;
+      if (E != 0) {                                // uniform: some row's reference must move
 #pragma unroll
-      for (int r = 0; r < 16; ++r) {
-        const float bm = fmaxf(fmaxf(red[sb][0][r], red[sb][1][r]), fmaxf(red[sb][2][r], red[sb][3][r]));
-        mt[r] = fmaxf(mt[r], bm);
-        alpha[r] = 1.0f;
-        if (bm > m[r] + kRescale) {
-          if (m[r] > -INFINITY) { alpha[r] = exp2f(m[r] - bm); need = true; }
-          m[r] = bm;
+        for (int r = 0; r < 16; ++r) {
+          if ((E >> r) & 1u) {
+            float mr = x[r];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mr = fmaxf(mr, __shfl_xor_sync(0xffffffffu, mr, o));
+            if (lane == 0) red[sb][q4][r] = mr;
+          }
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+          alpha[r] = 1.0f;
+          if ((E >> r) & 1u) {
+            const float bm = fmaxf(fmaxf(red[sb][0][r], red[sb][1][r]), fmaxf(red[sb][2][r], red[sb][3][r])) - kDecHead;
+            if (m[r] > -INFINITY) { alpha[r] = exp2f(m[r] - bm); need = true; }
+            m[r] = bm;
+          }
         }
       }
       // P buffer sb is free once PV_{jj-2} is done (also bounds the pv parity below)
       mbar_wait_ab(&bar_pe[sb], ph ^ 1, err, &abort_s);
-      if (need) {                       // uniform: every thread holds the same m
+      if (need) {                                  // uniform: every thread holds the same m
         mbar_wait_ab(&bar_pv, (jj - 1) & 1, err, &abort_s);
         tc_fence_after();
         uint32_t o[16];
@@ -685,14 +716,28 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         tmem_st16(tmem + lane_off + 32, o);
         tc_fence_before();
       }
-      uint8_t* pb = smem + kDPOff + sb * 4096;
-      const uint32_t pofs = (key >> 6) * 2048;
-      const uint32_t cc = (key & 63) >> 3, e2 = (key & 7) * 2;
+      // P -> three e4m3 terms, into row r, column `key` of each operand
+      uint8_t* pbuf = smem + kDPOff + sb * 6144;
+      const uint32_t kc = uint32_t(key >> 4), kb = uint32_t(key & 15);
 #pragma unroll
-      for (int r = 0; r < 16; ++r) {
-        const float p = fast_exp2(x[r] - (m[r] == -INFINITY ? 0.f : m[r]));
-        ls[r] += p;
-        *reinterpret_cast<__half*>(pb + pofs + swz_offset(r, cc, 128) + e2) = __float2half_rn(p);
+      for (int r = 0; r < 16; r += 2) {
+        float p0 = fast_exp2(x[r] - (m[r] == -INFINITY ? 0.f : m[r]));
+        float p1 = fast_exp2(x[r + 1] - (m[r + 1] == -INFINITY ? 0.f : m[r + 1]));
+        ls[r] += p0;
+        ls[r + 1] += p1;
+        const uint32_t o0 = swz_offset(uint32_t(r), kc, 128) + kb, o1 = swz_offset(uint32_t(r + 1), kc, 128) + kb;
+#pragma unroll
+        for (int part = 0; part < 3; ++part) {
+          const uint16_t e = e4m3x2_from_f32(p0, p1);
+          pbuf[part * 2048 + o0] = uint8_t(e & 0xFF);
+          pbuf[part * 2048 + o1] = uint8_t(e >> 8);
+          if (part < 2) {                          // the remainder is exact in fp32
+            const uint32_t eh = e4m3x2_to_f16x2(e);
+            const float2 ef = __half22float2(*reinterpret_cast<const __half2*>(&eh));
+            p0 -= ef.x;
+            p1 -= ef.y;
+          }
+        }
       }
       fence_async_shared();
       __syncwarp();
@@ -704,18 +749,25 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     uint32_t o[16];
     tmem_ld16(tmem + lane_off + 32, o);
     const size_t base = (unit * max_chunks + c) * G;
-    for (int r = 0; r < G; ++r) part_o[(base + r) * 128 + key] = __uint_as_float(o[r]);
+#pragma unroll
+    for (int r = 0; r < 16; ++r)
+      if (r < G) part_o[(base + r) * 128 + key] = __uint_as_float(o[r]);
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
-      float sr = ls[r];
+      float sr = ls[r], mr = mt[r];
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) sr += __shfl_xor_sync(0xffffffffu, sr, off);
-      if (lane == 0) lsum[q4][r] = sr;
+      for (int off = 16; off > 0; off >>= 1) {
+        sr += __shfl_xor_sync(0xffffffffu, sr, off);
+        mr = fmaxf(mr, __shfl_xor_sync(0xffffffffu, mr, off));
+      }
+      if (lane == 0) { red[0][q4][r] = sr; red[1][q4][r] = mr; }
     }
     asm volatile("bar.sync 1, 128;" ::: "memory");
     if (tid - 64 < G) {
       const int r = tid - 64;
-      part_s[base + r] = DecodePartial{m[r], lsum[0][r] + lsum[1][r] + lsum[2][r] + lsum[3][r], mt[r], 0.f};
+      part_s[base + r] = DecodePartial{m[r], red[0][0][r] + red[0][1][r] + red[0][2][r] + red[0][3][r],
+                                       fmaxf(fmaxf(red[1][0][r], red[1][1][r]), fmaxf(red[1][2][r], red[1][3][r])),
+                                       0.f};
     }
   }
   tc_fence_before();
@@ -789,13 +841,13 @@ cudaError_t launch_decode(const AttnArgs& a, cudaStream_t stream, const char** w
     if (!encode_tensor_map(&tm_k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.k_cache, dims, strides, box,
                            CU_TENSOR_MAP_SWIZZLE_128B, why) ||
         !encode_tensor_map(&tm_v, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.v_cache, dims, strides, box,
-                           CU_TENSOR_MAP_SWIZZLE_NONE, why))
+                           CU_TENSOR_MAP_SWIZZLE_128B, why))
       return cudaErrorInvalidValue;
   }
   cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecodeSmem);
   if (e != cudaSuccess) return e;
   profile_mark(stream, 0);
-  attn_decode_kernel<<<a.T * a.Hkv * mc, 320, kDecodeSmem, stream>>>(
+  attn_decode_kernel<<<a.T * a.Hkv * mc, 192, kDecodeSmem, stream>>>(
       tm_q, tm_k, tm_v, a.page_table, a.seq_lens, a.cu_q, a.topk, a.c_qk * kLog2e, a.B, a.T, a.Hq,
       a.Hkv, a.Hidx, a.topk_k, a.max_pages, a.num_pages, mc, part_o, part_s, n_chunks, a.err);
   profile_mark(stream, 1);

@@ -316,6 +316,13 @@ MSA_DEV uint32_t e4m3x2_to_f16x2(uint16_t x) {
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(x));
   return r;
 }
+// Two fp32 -> e4m3x2 (round to nearest even, saturating to +-448), `lo` in
+// the low byte.
+MSA_DEV uint16_t e4m3x2_from_f32(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
 // Two fp32 -> f16x2 (round to nearest even), `lo` in the low half.
 MSA_DEV uint32_t pack_f16x2(float lo, float hi) {
   uint32_t r;

@@ -154,3 +154,41 @@ def test_decode_config_sampled(msa):
     got = (o.float().cpu().numpy()[seqs].astype(np.float64), ml.cpu().numpy()[seqs],
            lse.cpu().numpy()[seqs])
     _check(got, ref)
+
+
+def _poison_tails(w, k8, v8):
+    """Copies of the K/V pools whose rows past each sequence's length, in its
+    last page, are e4m3 NaN (0x7F): positions >= seq_len are not part of the
+    sequence, so the result must not depend on them."""
+    kp, vp = k8.copy(), v8.copy()
+    for b in range(w.cfg.B):
+        L = int(w.seq_lens[b])
+        if L % 128:
+            page = w.page_table[b, (L - 1) // 128]
+            kp[page, :, L % 128:, :] = 0x7F
+            vp[page, :, L % 128:, :] = 0x7F
+    return kp, vp
+
+
+@pytest.mark.parametrize("kind", ["decode", "prefill"])
+def test_nan_past_seq_len_is_ignored(msa, kind):
+    if kind == "decode":
+        cfg = wl.GQAConfig("decnan", 12, (), 1, 16, 2, 4, 128, 128, 8, "channel",
+                           len_range=(1, 2000), max_pages=16, pool_factor=1.2, seed=31)
+    else:
+        cfg = wl.GQAConfig("prenan", 3, (200, 77, 301), 0, 8, 2, 2, 128, 64, 4, "normal",
+                           max_pages=8, pool_factor=1.0, seed=32)
+    w = wl.make_gqa(cfg)
+    assert np.any(w.seq_lens % 128)
+    ids = wl.random_topk(8, w.seq_lens, w.cu_q, w.cfg.Hidx, w.cfg.topk)
+    q8, k8, v8 = _codes(w)
+    kp, vp = _poison_tails(w, k8, v8)
+    o, ml, lse = msa.sparse_attn_fwd(dev(q8), dev(kp), dev(vp), dev(w.page_table), dev(w.seq_lens),
+                                     dev(w.cu_q), dev(ids), dev(w.sink), w.sm_scale, w.scales["q"],
+                                     w.scales["k"], w.scales["v"], w.max_q_len)
+    msa.check_errors()
+    got = (o.float().cpu().numpy().astype(np.float64), ml.cpu().numpy(), lse.cpu().numpy())
+    assert np.all(np.isfinite(got[0]))
+    ref = oa.sparse_attention(q8, k8, v8, w.page_table, w.seq_lens, w.cu_q, ids, w.sink, w.sm_scale,
+                              w.scales["q"], w.scales["k"], w.scales["v"])
+    _check(got, ref)
