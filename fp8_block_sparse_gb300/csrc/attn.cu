@@ -226,39 +226,39 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         bulk_load(smem + kVOff + s * 32768,
                   vt_img + ((size_t(ti.b) * max_pages + blk) * Hkv + g) * 32768, 32768, &bar_vf[s]);
       }
-    } else if (warp == 1 && lane == 0 && nU > 0 && mbar_wait_ab(&bar_q, 0, err, &abort_s)) {
-      // ---------------- MMA issue
+    } else if (warp == 1 && nU > 0 && mbar_wait_warp(&bar_q, 0, err, &abort_s)) {
+      // ---------------- MMA issue (whole warp, one elected lane per instruction)
       const uint32_t sq = smem_addr(smem + kQOff);
       auto issue_s = [&](int j, int x) -> bool {
         const int s = j % kStages;
-        if (x == 0 && !mbar_wait_ab(&bar_kf[s], (j / kStages) & 1, err, &abort_s)) return false;
+        if (x == 0 && !mbar_wait_warp(&bar_kf[s], (j / kStages) & 1, err, &abort_s)) return false;
         tc_fence_after();
         const uint32_t sk = smem_addr(smem + kKOff + s * 16384);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          mma_e4m3(tmem + x * 128, sdesc_kmajor(sq + x * 16384 + 32 * k, 128),
-                   sdesc_kmajor(sk + 32 * k, 128), kIdescQK, k > 0);
-        mma_commit(&bar_sf[x]);
-        if (x == 1) mma_commit(&bar_ke[s]);
+          mma_e4m3_w(tmem + x * 128, sdesc_kmajor(sq + x * 16384 + 32 * k, 128),
+                     sdesc_kmajor(sk + 32 * k, 128), kIdescQK, k > 0);
+        mma_commit_w(&bar_sf[x]);
+        if (x == 1) mma_commit_w(&bar_ke[s]);
         return true;
       };
       bool ok = issue_s(0, 0) && issue_s(0, 1);
       for (int j = 0; ok && j < nU; ++j) {
         const int s = j % kStages;
-        if (!mbar_wait_ab(&bar_vf[s], (j / kStages) & 1, err, &abort_s)) break;
+        if (!mbar_wait_warp(&bar_vf[s], (j / kStages) & 1, err, &abort_s)) break;
         const uint32_t sv = smem_addr(smem + kVOff + s * 32768);
         for (int x = 0; x < 2; ++x) {
-          if (!(ok = mbar_wait_ab(&bar_pf[x], j & 1, err, &abort_s))) break;
+          if (!(ok = mbar_wait_warp(&bar_pf[x], j & 1, err, &abort_s))) break;
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            mma_f16_ts(tmem + 256 + x * 128, tmem + x * 128 + 8 * k,
-                       sdesc_kmajor(sv + (k >> 2) * 16384 + (k & 3) * 32, 128), kIdescPV,
-                       (j > 0 || k > 0) ? 1u : 0u);
-          if (x == 1) mma_commit(&bar_ve[s]);
+            mma_f16_ts_w(tmem + 256 + x * 128, tmem + x * 128 + 8 * k,
+                         sdesc_kmajor(sv + (k >> 2) * 16384 + (k & 3) * 32, 128), kIdescPV,
+                         (j > 0 || k > 0) ? 1u : 0u);
+          if (x == 1) mma_commit_w(&bar_ve[s]);
           if (j + 1 < nU && !(ok = issue_s(j + 1, x))) break;
         }
-        if (ok && j == nU - 1) mma_commit(&bar_done);
+        if (ok && j == nU - 1) mma_commit_w(&bar_done);
       }
     }
   } else {
@@ -274,7 +274,11 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       const bool sel = row_valid && next_id == blk;
       if (sel) {
         ++ptr;
-        next_id = ptr < topk_k ? __ldg(src + ptr) : -1;
+        // issued here, consumed a block later (volatile: kept ahead of the waits)
+        int nid = -1;
+        if (ptr < topk_k)
+          asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(nid) : "l"(src + ptr));
+        next_id = nid;
       }
       const int ncol = !sel ? 0 : (blk < own ? 128 : pos - blk * 128 + 1);
       // S_X(j) done (and with it PV_X(j-1): O is settled and P may be rewritten)

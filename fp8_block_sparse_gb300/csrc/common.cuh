@@ -309,6 +309,56 @@ MSA_DEV void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
       : "memory");
 }
 
+// ---------------------------------------------------------------- warp-issued tcgen05
+// The same MMAs and commits issued by a whole converged warp, with one lane
+// elected inside the instruction sequence. Keeping the issuing loop
+// converged lets the compiler hold descriptors and addresses in warp-uniform
+// registers; a loop run by lane 0 alone measurably slows every issue and
+// turns each commit into a stall.
+MSA_DEV void mma_e4m3_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+MSA_DEV void mma_e4m3_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+MSA_DEV void mma_f16_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+MSA_DEV void mma_f16_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+MSA_DEV void mma_commit_w(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+          smem_addr(bar))
+      : "memory");
+}
+// mbar_wait_ab for a whole converged warp; the result is the same in every lane.
+MSA_DEV bool mbar_wait_warp(uint64_t* bar, uint32_t parity, unsigned* err, volatile int* abort) {
+  return __all_sync(0xffffffffu, mbar_wait_ab(bar, parity, err, abort));
+}
+
 // ---------------------------------------------------------------- misc
 // Two e4m3 codes (low byte first) -> two f16 (exact: every e4m3 value is an f16).
 MSA_DEV uint32_t e4m3x2_to_f16x2(uint16_t x) {
