@@ -610,28 +610,28 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       }
     }
   } else if (warp == 1) {
-    if (lane == 0 && mbar_wait_ab(&bar_q, 0, err, &abort_s)) {
+    if (mbar_wait_warp(&bar_q, 0, err, &abort_s)) {        // whole warp, elected issue
       const uint32_t sq = smem_addr(smem + kDQOff);
       auto issue_s = [&](int jj) -> bool {
         const int s = jj % kDecKStages, sb = jj & 1;
-        if (!mbar_wait_ab(&bar_kf[s], (jj / kDecKStages) & 1, err, &abort_s)) return false;
-        if (!mbar_wait_ab(&bar_se[sb], ((jj >> 1) & 1) ^ 1, err, &abort_s)) return false;
+        if (!mbar_wait_warp(&bar_kf[s], (jj / kDecKStages) & 1, err, &abort_s)) return false;
+        if (!mbar_wait_warp(&bar_se[sb], ((jj >> 1) & 1) ^ 1, err, &abort_s)) return false;
         tc_fence_after();
         const uint32_t sk = smem_addr(smem + kDKOff + s * 16384);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          mma_e4m3(tmem + sb * 16, sdesc_kmajor(sk + 32 * k, 128), sdesc_kmajor(sq + 32 * k, 128),
+          mma_e4m3_w(tmem + sb * 16, sdesc_kmajor(sk + 32 * k, 128), sdesc_kmajor(sq + 32 * k, 128),
                    kIdescDec, k > 0);
-        mma_commit(&bar_ke[s]);
-        mma_commit(&bar_sf[sb]);
+        mma_commit_w(&bar_ke[s]);
+        mma_commit_w(&bar_sf[sb]);
         return true;
       };
       bool ok = n > 0 && issue_s(0);
       for (int jj = 0; ok && jj < n; ++jj) {
         if (jj + 1 < n && !(ok = issue_s(jj + 1))) break;
         const int s = jj % kDecVStages, sb = jj & 1;
-        if (!mbar_wait_ab(&bar_pf[sb], (jj >> 1) & 1, err, &abort_s) ||
-            !mbar_wait_ab(&bar_vf[s], (jj / kDecVStages) & 1, err, &abort_s))
+        if (!mbar_wait_warp(&bar_pf[sb], (jj >> 1) & 1, err, &abort_s) ||
+            !mbar_wait_warp(&bar_vf[s], (jj / kDecVStages) & 1, err, &abort_s))
           break;
         tc_fence_after();
         const uint32_t sv = smem_addr(smem + kDVOff + s * 16384);
@@ -640,13 +640,13 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         for (int part = 0; part < 3; ++part)          // the three terms of P
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_e4m3(tmem + 32, sdesc_kmajor(sv + 4096 * k, 128),
+            mma_e4m3_w(tmem + 32, sdesc_kmajor(sv + 4096 * k, 128),
                      sdesc_kmajor(sp + part * 2048 + 32 * k, 128), kIdescDecT,
                      (jj > 0 || part > 0 || k > 0) ? 1u : 0u);
-        mma_commit(&bar_ve[s]);
-        mma_commit(&bar_pe[sb]);
-        mma_commit(&bar_pv);
-        if (jj == n - 1) mma_commit(&bar_done);
+        mma_commit_w(&bar_ve[s]);
+        mma_commit_w(&bar_pe[sb]);
+        mma_commit_w(&bar_pv);
+        if (jj == n - 1) mma_commit_w(&bar_done);
       }
     }
   } else {

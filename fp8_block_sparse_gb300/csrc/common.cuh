@@ -354,6 +354,10 @@ MSA_DEV void mma_commit_w(uint64_t* bar) {
           smem_addr(bar))
       : "memory");
 }
+// mbar_wait for a whole converged warp; the result is the same in every lane.
+MSA_DEV bool mbar_wait_warp(uint64_t* bar, uint32_t parity, unsigned* err) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, err));
+}
 // mbar_wait_ab for a whole converged warp; the result is the same in every lane.
 MSA_DEV bool mbar_wait_warp(uint64_t* bar, uint32_t parity, unsigned* err, volatile int* abort) {
   return __all_sync(0xffffffffu, mbar_wait_ab(bar, parity, err, abort));

@@ -113,19 +113,19 @@ index_score_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
       }
     }
   } else if (warp == 1) {
-    if (lane == 0 && mbar_wait(&bar_q, 0, err)) {
+    if (mbar_wait_warp(&bar_q, 0, err)) {          // whole warp, elected issue
       for (int j = 0; j < nblk; ++j) {
         const int s = j % kStages, buf = j & 1;
-        if (!mbar_wait(&bar_full[s], (j / kStages) & 1, err)) break;
-        if (!mbar_wait(&bar_tempty[buf], ((j >> 1) & 1) ^ 1, err)) break;
+        if (!mbar_wait_warp(&bar_full[s], (j / kStages) & 1, err)) break;
+        if (!mbar_wait_warp(&bar_tempty[buf], ((j >> 1) & 1) ^ 1, err)) break;
         tc_fence_after();
         const uint32_t aq = smem_addr(sQ), bk = smem_addr(sK + s * 16384);
 #pragma unroll
         for (int k = 0; k < D / 32; ++k)
-          mma_e4m3(tmem + buf * 128, sdesc_kmajor(aq + 32 * k, SWZ), sdesc_kmajor(bk + 32 * k, SWZ),
-                   kIdesc, k > 0);
-        mma_commit(&bar_empty[s]);
-        mma_commit(&bar_tfull[buf]);
+          mma_e4m3_w(tmem + buf * 128, sdesc_kmajor(aq + 32 * k, SWZ), sdesc_kmajor(bk + 32 * k, SWZ),
+                     kIdesc, k > 0);
+        mma_commit_w(&bar_empty[s]);
+        mma_commit_w(&bar_tfull[buf]);
       }
     }
   } else {
@@ -226,19 +226,19 @@ index_score_decode_kernel(const __grid_constant__ CUtensorMap tm_q,
       }
     }
   } else if (warp == 1) {
-    if (lane == 0 && mbar_wait(&bar_q, 0, err)) {
+    if (mbar_wait_warp(&bar_q, 0, err)) {          // whole warp, elected issue
       for (int j = 0; j < nblk; ++j) {
         const int s = j % kStages, buf = j % kBufs;
-        if (!mbar_wait(&bar_full[s], (j / kStages) & 1, err)) break;
-        if (!mbar_wait(&bar_tempty[buf], ((j / kBufs) & 1) ^ 1, err)) break;
+        if (!mbar_wait_warp(&bar_full[s], (j / kStages) & 1, err)) break;
+        if (!mbar_wait_warp(&bar_tempty[buf], ((j / kBufs) & 1) ^ 1, err)) break;
         tc_fence_after();
         const uint32_t ak = smem_addr(sK + s * 16384), bq = smem_addr(sQ);
 #pragma unroll
         for (int k = 0; k < D / 32; ++k)
-          mma_e4m3(tmem + buf * 16, sdesc_kmajor(ak + 32 * k, SWZ), sdesc_kmajor(bq + 32 * k, SWZ),
-                   kIdesc, k > 0);
-        mma_commit(&bar_empty[s]);
-        mma_commit(&bar_tfull[buf]);
+          mma_e4m3_w(tmem + buf * 16, sdesc_kmajor(ak + 32 * k, SWZ), sdesc_kmajor(bq + 32 * k, SWZ),
+                     kIdesc, k > 0);
+        mma_commit_w(&bar_empty[s]);
+        mma_commit_w(&bar_tfull[buf]);
       }
     }
   } else {

@@ -93,30 +93,33 @@ mla_prefill_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_con
   const uint32_t tmem = tmem_base_s;          // S buffers at cols 0 and 64; O at 256
 
   if (warp == 0) {
-    // ---------------- Q (one TMA batch) and MMA issue
-    if (lane == 0 && nch > 0) {
-      mbar_arrive_expect_tx(&bar_q, 128 * kDqk);
-      for (int r = 0; r < 4; ++r) tma_load_2d(smem + kQOff + r * 16384, &tm_q128, &bar_q, r * 128, t * 128);
-      tma_load_2d(smem + kQTail, &tm_q64, &bar_q, 512, t * 128);
-      if (mbar_wait_ab(&bar_q, 0, err, &abort_s)) {
+    // ---------------- Q (one TMA batch), then MMA issue (whole warp, elected lane)
+    if (nch > 0) {
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bar_q, 128 * kDqk);
+        for (int r = 0; r < 4; ++r) tma_load_2d(smem + kQOff + r * 16384, &tm_q128, &bar_q, r * 128, t * 128);
+        tma_load_2d(smem + kQTail, &tm_q64, &bar_q, 512, t * 128);
+      }
+      __syncwarp();
+      if (mbar_wait_warp(&bar_q, 0, err, &abort_s)) {
         const uint32_t sq = smem_addr(smem + kQOff);
         auto issue_s = [&](int j) -> bool {
           const int s = j & 1;
           const uint32_t ph = (j >> 1) & 1;
-          if (!mbar_wait_ab(&bar_kf[s], ph, err, &abort_s)) return false;
-          if (!mbar_wait_ab(&bar_se[s], ph ^ 1, err, &abort_s)) return false;
+          if (!mbar_wait_warp(&bar_kf[s], ph, err, &abort_s)) return false;
+          if (!mbar_wait_warp(&bar_se[s], ph ^ 1, err, &abort_s)) return false;
           tc_fence_after();
           const uint32_t sk = smem_addr(smem + kKOff + s * kKStage);
 #pragma unroll
           for (int k = 0; k < 16; ++k)
-            mma_e4m3(tmem + s * 64, sdesc_kmajor(sq + (k >> 2) * 16384 + (k & 3) * 32, 128),
-                     sdesc_kmajor(sk + (k >> 2) * 8192 + (k & 3) * 32, 128), kIdescQK, k > 0);
+            mma_e4m3_w(tmem + s * 64, sdesc_kmajor(sq + (k >> 2) * 16384 + (k & 3) * 32, 128),
+                       sdesc_kmajor(sk + (k >> 2) * 8192 + (k & 3) * 32, 128), kIdescQK, k > 0);
 #pragma unroll
           for (int k = 0; k < 2; ++k)
-            mma_e4m3(tmem + s * 64, sdesc_kmajor(sq + kQTail + k * 32, 64),
-                     sdesc_kmajor(sk + kKTail + k * 32, 64), kIdescQK, 1u);
-          mma_commit(&bar_ke[s]);
-          mma_commit(&bar_sf[s]);
+            mma_e4m3_w(tmem + s * 64, sdesc_kmajor(sq + kQTail + k * 32, 64),
+                       sdesc_kmajor(sk + kKTail + k * 32, 64), kIdescQK, 1u);
+          mma_commit_w(&bar_ke[s]);
+          mma_commit_w(&bar_sf[s]);
           return true;
         };
         bool ok = issue_s(0);
@@ -124,17 +127,17 @@ mla_prefill_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_con
           if (j + 1 < nch && !(ok = issue_s(j + 1))) break;
           const int s = j & 1;
           const uint32_t ph = (j >> 1) & 1;
-          if (!mbar_wait_ab(&bar_pf[s], ph, err, &abort_s) || !mbar_wait_ab(&bar_vtf, j & 1, err, &abort_s)) break;
+          if (!mbar_wait_warp(&bar_pf[s], ph, err, &abort_s) || !mbar_wait_warp(&bar_vtf, j & 1, err, &abort_s)) break;
           tc_fence_after();
           const uint32_t sp = smem_addr(smem + kPOff + s * 16384), svt = smem_addr(smem + kVTOff);
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_f16(tmem + 256, sdesc_kmajor(sp + k * 32, 128), sdesc_kmajor(svt + k * 32, 128), kIdescPV,
-                    (j > 0 || k > 0) ? 1u : 0u);
-          mma_commit(&bar_vte);
-          mma_commit(&bar_pe[s]);
-          mma_commit(&bar_pv);
-          if (j == nch - 1) mma_commit(&bar_done);
+            mma_f16_w(tmem + 256, sdesc_kmajor(sp + k * 32, 128), sdesc_kmajor(svt + k * 32, 128), kIdescPV,
+                      (j > 0 || k > 0) ? 1u : 0u);
+          mma_commit_w(&bar_vte);
+          mma_commit_w(&bar_pe[s]);
+          mma_commit_w(&bar_pv);
+          if (j == nch - 1) mma_commit_w(&bar_done);
         }
       }
     }
