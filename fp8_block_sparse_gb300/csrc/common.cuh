@@ -201,6 +201,16 @@ MSA_DEV uint64_t sdesc_kmajor(uint32_t saddr, uint32_t swz) {
          (uint64_t(((8u * swz) >> 4) & 0x3FFFu) << 32) | (uint64_t(1) << 46) | (layout << 61);
 }
 
+// Shared-memory matrix descriptor for an MN-major operand in the 128-byte
+// swizzled layout: rows of 128 bytes along M/N (64 f16 or 128 e4m3), one row
+// per K index, 8-row groups 1024 bytes apart along K, and successive 128-byte
+// wide column blocks of M/N `mn_stride` bytes apart. Select it with the
+// transpose bit of the instruction descriptor (bit 15 for A, 16 for B).
+MSA_DEV uint64_t sdesc_mn_sw128(uint32_t saddr, uint32_t mn_stride) {
+  return uint64_t((saddr >> 4) & 0x3FFFu) | (uint64_t((mn_stride >> 4) & 0x3FFFu) << 16) |
+         (uint64_t(1024 >> 4) << 32) | (uint64_t(1) << 46) | (uint64_t(2) << 61);
+}
+
 // Byte offset of the 16-byte chunk `c` of row `r` inside a swizzled K-major
 // region with `swz`-byte rows (the layout TMA writes with the same swizzle):
 // address bits [4, 4+n) are XOR-ed with bits [7, 7+n), n = log2(swz/16).

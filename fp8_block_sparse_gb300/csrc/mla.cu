@@ -22,11 +22,12 @@
 //            one 64-byte swizzled region for the last 64 columns; invalid
 //            entries become zero rows (and are masked);
 //   S = Q K^T  tcgen05 e4m3, M=128, N=64, K=576 (18 MMAs), double-buffered TMEM;
-//   V^T      the same warps turn this CTA's 256 V columns of the tile into an
-//            f16 V^T operand (rows = d, K = keys);
+//   V        the same warps widen this CTA's 256 V columns of the tile to
+//            f16 in place of layout (rows = keys, 16-byte loads, two 16-byte
+//            stores each, no transpose); PV reads it as an MN-major operand;
 //   P        one thread per head row: online softmax with lazy rescale, P in
 //            f16 (e4m3 P costs ~2.5% relative error on flat rows);
-//   O += P V tcgen05 kind::f16, M=128, N=256, K=64.
+//   O += P V tcgen05 kind::f16, M=128, N=256, K=64, B (V) MN-major.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -47,12 +48,13 @@ constexpr int kQTail = 65536;
 constexpr int kKOff = 73728;        // 2 stages x 36 KB: 4 x 8 KB (SW128) + 4 KB (SW64)
 constexpr int kKStage = 36864;
 constexpr int kKTail = 32768;       // offset of the SW64 region inside a stage
-constexpr int kVTOff = 147456;      // 256 x 64 f16 V^T (one 128-byte swizzle column)
-constexpr int kPOff = 180224;       // 2 x (128 x 64 f16)
+constexpr int kVTOff = 147456;      // 2 x (64 keys x 256 f16 V: 4 blocks of 64 columns, 8 KB each, SW128)
 constexpr int kMlaSmem = 212992 + 1024;
+// TMEM columns: S_s at 64*s, P_s (f16 pairs) at 128 + 32*s, O at 256
+constexpr uint32_t kTP = 128, kTO = 256;
 
 constexpr uint32_t kIdescQK = idesc_f32(128, 64);
-constexpr uint32_t kIdescPV = idesc_f32(128, 256);
+constexpr uint32_t kIdescPV = idesc_f32(128, 256) | (1u << 16);   // B MN-major
 
 __global__ void __launch_bounds__(288, 1)
 mla_prefill_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_constant__ CUtensorMap tm_q64,
@@ -64,7 +66,7 @@ mla_prefill_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_con
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   __shared__ uint64_t bar_q, bar_kf[2], bar_ke[2], bar_sf[2], bar_se[2], bar_pf[2], bar_pe[2],
-      bar_vtf, bar_vte, bar_pv, bar_done;
+      bar_vtf[2], bar_vte[2], bar_pv, bar_done;
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_s;
 
@@ -82,15 +84,15 @@ mla_prefill_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_con
       mbar_init(&bar_kf[s], 1); mbar_init(&bar_ke[s], 5);
       mbar_init(&bar_sf[s], 1); mbar_init(&bar_se[s], 4);
       mbar_init(&bar_pf[s], 4); mbar_init(&bar_pe[s], 1);
+      mbar_init(&bar_vtf[s], 4); mbar_init(&bar_vte[s], 1);
     }
-    mbar_init(&bar_vtf, 4); mbar_init(&bar_vte, 1);
     mbar_init(&bar_pv, 1); mbar_init(&bar_done, 1);
     fence_barrier_init();
   }
   if (warp == 0) { tmem_alloc(&tmem_base_s, 512); tmem_relinquish(); }
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = tmem_base_s;          // S buffers at cols 0 and 64; O at 256
+  const uint32_t tmem = tmem_base_s;
 
   if (warp == 0) {
     // ---------------- Q (one TMA batch), then MMA issue (whole warp, elected lane)
@@ -127,14 +129,14 @@ mla_prefill_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_con
           if (j + 1 < nch && !(ok = issue_s(j + 1))) break;
           const int s = j & 1;
           const uint32_t ph = (j >> 1) & 1;
-          if (!mbar_wait_warp(&bar_pf[s], ph, err, &abort_s) || !mbar_wait_warp(&bar_vtf, j & 1, err, &abort_s)) break;
+          if (!mbar_wait_warp(&bar_pf[s], ph, err, &abort_s) || !mbar_wait_warp(&bar_vtf[s], ph, err, &abort_s)) break;
           tc_fence_after();
-          const uint32_t sp = smem_addr(smem + kPOff + s * 16384), svt = smem_addr(smem + kVTOff);
+          const uint32_t svt = smem_addr(smem + kVTOff + s * 32768);
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_f16_w(tmem + 256, sdesc_kmajor(sp + k * 32, 128), sdesc_kmajor(svt + k * 32, 128), kIdescPV,
-                      (j > 0 || k > 0) ? 1u : 0u);
-          mma_commit_w(&bar_vte);
+          for (int k = 0; k < 4; ++k)            // 16 keys per step: 8 P columns, 16 V rows of 128 bytes
+            mma_f16_ts_w(tmem + kTO, tmem + kTP + 32 * s + 8 * k, sdesc_mn_sw128(svt + k * 2048, 8192),
+                         kIdescPV, (j > 0 || k > 0) ? 1u : 0u);
+          mma_commit_w(&bar_vte[s]);
           mma_commit_w(&bar_pe[s]);
           mma_commit_w(&bar_pv);
           if (j == nch - 1) mma_commit_w(&bar_done);
@@ -142,25 +144,42 @@ mla_prefill_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_con
       }
     }
   } else if (warp <= 4) {
-    // ---------------- producers: gather chunk j, convert chunk j-1
-    const int pt = tid - 32;
-    const int r = pt >> 1, part = pt & 1;
+    // ---------------- producers: gather chunk j, widen chunk j-1
+    // Gather: producer warp pw copies rows 16*pw .. 16*pw+15 of the chunk, one
+    // row at a time with all 32 lanes (576 bytes = 36 chunks of 16 bytes), so
+    // every cp.async instruction reads contiguous bytes of one kv row.
+    const int pt = tid - 32, pw = pt >> 5;
+    // lanes 0..15 hold the kv index of row 16*pw + lane, loaded one chunk ahead
+    int idx_next = -1;
+    if (lane < 16 && pw * 16 + lane < len)
+      asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(idx_next) : "l"(idx_row + pw * 16 + lane));
     for (int j = 0; j <= nch; ++j) {
       if (j < nch) {
         const int s = j & 1;
+        int my_idx = idx_next;
+        const int key_n = (j + 1) * kChunkKeys + pw * 16 + lane;
+        idx_next = -1;
+        if (lane < 16 && key_n < len)
+          asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(idx_next) : "l"(idx_row + key_n));
+        if (lane < 16 && my_idx >= S_kv) { atomicOr(err, MSA_DEVERR_DATA); my_idx = -1; }
         mbar_wait_ab(&bar_ke[s], ((j >> 1) & 1) ^ 1, err, &abort_s);
-        const int key = j * kChunkKeys + r;
-        int idx = key < len ? __ldg(idx_row + key) : -1;
-        if (idx >= S_kv) { atomicOr(err, MSA_DEVERR_DATA); idx = -1; }
         uint8_t* stage = smem + kKOff + s * kKStage;
-        const uint8_t* src = kv + size_t(idx < 0 ? 0 : idx) * kDqk;
-#pragma unroll
-        for (int cc = 0; cc < 18; ++cc) {
-          const int c = part * 18 + cc;
-          uint8_t* dst = c < 32 ? stage + (c >> 3) * 8192 + swz_offset(r, c & 7, 128)
-                                : stage + kKTail + swz_offset(r, c - 32, 64);
-          if (idx >= 0) cp_async16(dst, src + c * 16);
-          else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll 4
+        for (int rr = 0; rr < 16; ++rr) {
+          const int r = pw * 16 + rr;
+          const int idx = __shfl_sync(0xffffffffu, my_idx, rr);
+          const uint8_t* src = kv + size_t(idx < 0 ? 0 : idx) * kDqk;
+          {
+            const int c = lane;                                  // chunks 0..31: SW128 regions
+            uint8_t* dst = stage + (c >> 3) * 8192 + swz_offset(r, c & 7, 128);
+            if (idx >= 0) cp_async16(dst, src + c * 16);
+            else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+          }
+          if (lane < 4) {                                        // chunks 32..35: SW64 tail
+            uint8_t* dst = stage + kKTail + swz_offset(r, lane, 64);
+            if (idx >= 0) cp_async16(dst, src + (32 + lane) * 16);
+            else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+          }
         }
         cp_async_commit();
       }
@@ -170,29 +189,30 @@ mla_prefill_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_con
         fence_async_shared();
         asm volatile("bar.sync 2, 128;" ::: "memory");        // chunk jp has landed
         if (pt == 0) mbar_arrive(&bar_kf[sp]);
-        // V^T for this CTA's d_v half: row d (0..255), 16-byte chunk = 8 keys
-        mbar_wait_ab(&bar_vte, (jp & 1) ^ 1, err, &abort_s);
+        // V for this CTA's d_v half as f16, rows = keys: item = (key, 16 columns)
+        mbar_wait_ab(&bar_vte[sp], ((jp >> 1) & 1) ^ 1, err, &abort_s);   // PV(jp-2) done
         const uint8_t* stage = smem + kKOff + sp * kKStage;
-        uint8_t* vt = smem + kVTOff;
+        uint8_t* vimg = smem + kVTOff + sp * 32768;
 #pragma unroll 2
-        for (int x = pt; x < 256 * 8; x += 128) {
-          const int dl = x & 255, c8 = x >> 8;
-          const int d = hf * 256 + dl;
-          const uint8_t* col = stage + (d >> 7) * 8192;
-          const int dc = (d & 127) >> 4, db = d & 15;
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int k0 = c8 * 8 + 2 * e;
-            const uint32_t lo = col[swz_offset(k0, dc, 128) + db];
-            const uint32_t hi = col[swz_offset(k0 + 1, dc, 128) + db];
-            w[e] = e4m3x2_to_f16x2(uint16_t(lo | (hi << 8)));
-          }
-          *reinterpret_cast<uint4*>(vt + swz_offset(dl, c8, 128)) = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int x = pt; x < kChunkKeys * 16; x += 128) {
+          const int kr = x >> 4, g16 = x & 15;
+          const int d0 = hf * 256 + g16 * 16;                   // first of 16 columns
+          const uint4 v = *reinterpret_cast<const uint4*>(stage + (d0 >> 7) * 8192 +
+                                                          swz_offset(kr, (d0 & 127) >> 4, 128));
+          uint4 lo4, hi4;
+          lo4.x = e4m3x2_to_f16x2(uint16_t(v.x)); lo4.y = e4m3x2_to_f16x2(uint16_t(v.x >> 16));
+          lo4.z = e4m3x2_to_f16x2(uint16_t(v.y)); lo4.w = e4m3x2_to_f16x2(uint16_t(v.y >> 16));
+          hi4.x = e4m3x2_to_f16x2(uint16_t(v.z)); hi4.y = e4m3x2_to_f16x2(uint16_t(v.z >> 16));
+          hi4.z = e4m3x2_to_f16x2(uint16_t(v.w)); hi4.w = e4m3x2_to_f16x2(uint16_t(v.w >> 16));
+          const int dl = g16 * 16;                               // local column 0..255
+          uint8_t* blk = vimg + (dl >> 6) * 8192;                // 64 f16 columns per 128-byte row
+          const uint32_t c0 = uint32_t(dl & 63) >> 3;
+          *reinterpret_cast<uint4*>(blk + swz_offset(kr, c0, 128)) = lo4;
+          *reinterpret_cast<uint4*>(blk + swz_offset(kr, c0 + 1, 128)) = hi4;
         }
         fence_async_shared();
         __syncwarp();
-        if (lane == 0) { mbar_arrive(&bar_vtf); mbar_arrive(&bar_ke[sp]); }
+        if (lane == 0) { mbar_arrive(&bar_vtf[sp]); mbar_arrive(&bar_ke[sp]); }
       }
     }
   } else {
@@ -201,18 +221,21 @@ mla_prefill_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_con
     const int row = q4 * 32 + lane;
     const uint32_t lane_off = uint32_t(q4 * 32) << 16;
     float m = -INFINITY, m_true = -INFINITY, l = 0.f;
+    // validity of the chunk's 64 keys: lane holds keys lane and lane + 32,
+    // loaded one chunk ahead and combined with two ballots
+    int ia = -1, ib = -1;
+    if (lane < len) asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(ia) : "l"(idx_row + lane));
+    if (lane + 32 < len) asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(ib) : "l"(idx_row + lane + 32));
     for (int j = 0; j < nch; ++j) {
       const int s = j & 1;
       const uint32_t ph = (j >> 1) & 1;
-      uint64_t valid = 0;
-#pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        const int4 iv = __ldg(reinterpret_cast<const int4*>(idx_row + j * kChunkKeys) + q);
-        const int base = j * kChunkKeys + q * 4;
-        valid |= uint64_t((iv.x >= 0 && iv.x < S_kv && base + 0 < len) ? 1 : 0) << (q * 4 + 0);
-        valid |= uint64_t((iv.y >= 0 && iv.y < S_kv && base + 1 < len) ? 1 : 0) << (q * 4 + 1);
-        valid |= uint64_t((iv.z >= 0 && iv.z < S_kv && base + 2 < len) ? 1 : 0) << (q * 4 + 2);
-        valid |= uint64_t((iv.w >= 0 && iv.w < S_kv && base + 3 < len) ? 1 : 0) << (q * 4 + 3);
+      const uint64_t valid = uint64_t(__ballot_sync(0xffffffffu, ia >= 0 && ia < S_kv)) |
+                             (uint64_t(__ballot_sync(0xffffffffu, ib >= 0 && ib < S_kv)) << 32);
+      {
+        const int k0 = (j + 1) * kChunkKeys + lane;
+        ia = -1; ib = -1;
+        if (k0 < len) asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(ia) : "l"(idx_row + k0));
+        if (k0 + 32 < len) asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(ib) : "l"(idx_row + k0 + 32));
       }
       mbar_wait_ab(&bar_sf[s], ph, err, &abort_s);
       tc_fence_after();
@@ -244,32 +267,27 @@ mla_prefill_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_con
 #pragma unroll 4
         for (int c = 0; c < 256; c += 16) {
           uint32_t v[16];
-          tmem_ld16(tmem + lane_off + 256 + c, v);
+          tmem_ld16(tmem + lane_off + kTO + c, v);
 #pragma unroll
           for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-          tmem_st16(tmem + lane_off + 256 + c, v);
+          tmem_st16(tmem + lane_off + kTO + c, v);
         }
         tc_fence_before();
         if (need) l *= alpha;
       }
       if (grow) m = mx;
       const float mref = (m == -INFINITY) ? 0.f : m;
-      uint8_t* pbuf = smem + kPOff + s * 16384;
+      uint32_t w[32];
       float sum = 0.f;
 #pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float p0 = fast_exp2(x[c8 * 8 + 2 * e] - mref);
-          const float p1 = fast_exp2(x[c8 * 8 + 2 * e + 1] - mref);
-          sum += p0 + p1;
-          w[e] = pack_f16x2(p0, p1);
-        }
-        *reinterpret_cast<uint4*>(pbuf + swz_offset(row, c8, 128)) = make_uint4(w[0], w[1], w[2], w[3]);
+      for (int c = 0; c < 64; c += 2) {
+        const float p0 = fast_exp2(x[c] - mref), p1 = fast_exp2(x[c + 1] - mref);
+        sum += p0 + p1;
+        w[c >> 1] = pack_f16x2(p0, p1);
       }
+      tmem_st32(tmem + lane_off + kTP + 32 * s, w);
       l += sum;
-      fence_async_shared();
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_pf[s]);
     }
@@ -287,7 +305,7 @@ mla_prefill_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_con
     for (int c = 0; c < 256; c += 32) {
       uint32_t v[32];
       if (nch > 0) {
-        tmem_ld32(tmem + lane_off + 256 + c, v);
+        tmem_ld32(tmem + lane_off + kTO + c, v);
       } else {
 #pragma unroll
         for (int e = 0; e < 32; ++e) v[e] = 0u;
