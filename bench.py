@@ -132,14 +132,23 @@ def src_hash(*names):
 
 
 def traffic_for(kernel_file: str, profile_name: str):
-    """DRAM bytes per launch from a committed ncu summary, if it matches the source."""
+    """DRAM bytes per launch from a committed ncu summary (markdown with the
+    lines `source_hash: ...` and `dram_bytes_per_launch: ...`), if the summary
+    was taken on the current kernel source; else None."""
     path = os.path.join(ROOT, "profiles", profile_name)
     if not os.path.exists(path):
         return None
-    d = json.load(open(path))
-    if d.get("source_hash") != src_hash(kernel_file, "common.cuh"):
+    fields = {}
+    for line in open(path):
+        if ":" in line:
+            k, v = line.split(":", 1)
+            fields[k.strip().strip("`* -")] = v.strip().strip("`* ")
+    if fields.get("source_hash") != src_hash(kernel_file, "common.cuh"):
         return None
-    return d.get("dram_bytes_per_launch")
+    try:
+        return float(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
 
 
 # ----------------------------------------------------------------- workloads
@@ -501,7 +510,7 @@ def native_arm(args):
     achieved = flops / (kern_ms / 1e3) / 1e12
     roof = {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
             "frac": achieved / fp8_peak,
-            "traffic": traffic_for("attn.cu", "attn_prefill_32k_traffic.json"),
+            "traffic": traffic_for("attn.cu", "attn_prefill_kernel_prefill32k_traffic.md"),
             "kernel": "attn_prefill_kernel",
             "peak_basis": f"{pk['source']} bf16 burst {pk['bf16_tflops']:.0f} TF/s x2 (nominal fp8/bf16 ratio)",
             "algorithmic_flop_per_launch": flops, "executed_flop_per_launch": exe,
@@ -546,7 +555,7 @@ def native_arm(args):
                   "attn_kernel": {"kernel": "attn_decode_kernel", "ms": kern_d,
                                   "gbs": kv_b / (kern_d / 1e3) / 1e9,
                                   "frac_of_hbm": kv_b / (kern_d / 1e3) / 1e9 / pk["hbm_gbs"],
-                                  "traffic": traffic_for("attn.cu", "attn_decode_traffic.json")},
+                                  "traffic": traffic_for("attn.cu", "attn_decode_kernel_decode_traffic.md")},
                   "algorithmic_bytes_per_step": total_b, "kv_union_blocks": union,
                   "peak_hbm_gbs": pk["hbm_gbs"], "peak_basis": pk["source"]}
         del ds
