@@ -451,7 +451,13 @@ __host__ __device__ inline int dec_max_chunks(int n_idx_per_group, int topk, int
   return max(1, (cap + kDecChunk - 1) / kDecChunk);
 }
 
-__global__ void __launch_bounds__(192, 2)
+constexpr int kDecThreads = 320;   // producer, MMA, 8 softmax warps
+
+// RPT = query rows per softmax thread: the 16 MMA columns (query rows) are
+// split between the two softmax warps of each TMEM lane quarter, rows
+// RPT*rh .. RPT*rh+RPT-1 for warp half rh; RPT = 4 when G <= 8.
+template <int RPT>
+__global__ void __launch_bounds__(kDecThreads, 2)
 attn_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const int32_t* __restrict__ page_table,
                    const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ cu_q,
@@ -466,8 +472,9 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
   __shared__ uint32_t tmem_base_s;
   __shared__ int n_union_s;
   __shared__ int abort_s;
-  __shared__ uint32_t flags[2][4];
+  __shared__ uint32_t flags[2][8];
   __shared__ float red[2][4][16];
+  __shared__ float mrow[16];
 
   const int G = Hq / Hkv;
   const int c = blockIdx.x % max_chunks;
@@ -491,9 +498,9 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
   int16_t* sList = reinterpret_cast<int16_t*>(smem + kDListOff);
   uint16_t* sMask = reinterpret_cast<uint16_t*>(smem + kDMaskOff);
   uint32_t* sBits = reinterpret_cast<uint32_t*>(smem + kDBitsOff);
-  for (int x = tid; x < n_idx * 64; x += 192) sBits[x] = 0u;
+  for (int x = tid; x < n_idx * 64; x += kDecThreads) sBits[x] = 0u;
   __syncthreads();
-  for (int x = tid; x < n_idx * topk_k; x += 192) {
+  for (int x = tid; x < n_idx * topk_k; x += kDecThreads) {
     const int il = x / topk_k;
     const int id = __ldg(topk + (size_t(i_first + il) * T + t) * topk_k + (x - il * topk_k));
     if (id < 0) continue;
@@ -548,8 +555,8 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     for (int s = 0; s < kDecKStages; ++s) { mbar_init(&bar_kf[s], 1); mbar_init(&bar_ke[s], 1); }
     for (int s = 0; s < kDecVStages; ++s) { mbar_init(&bar_vf[s], 1); mbar_init(&bar_ve[s], 1); }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&bar_sf[s], 1); mbar_init(&bar_se[s], 4);
-      mbar_init(&bar_pf[s], 4); mbar_init(&bar_pe[s], 1);
+      mbar_init(&bar_sf[s], 1); mbar_init(&bar_se[s], 8);
+      mbar_init(&bar_pf[s], 8); mbar_init(&bar_pe[s], 1);
     }
     mbar_init(&bar_pv, 1);
     mbar_init(&bar_done, 1);
@@ -650,13 +657,15 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       }
     }
   } else {
-    // ---------------- softmax: thread = key lane of S^T and d lane of O^T
-    const int q4 = warp & 3;
+    // ---------------- softmax: thread = key lane of S^T and d lane of O^T,
+    // query rows r0 .. r0+RPT-1
+    const int q4 = warp & 3, rh = (warp - 2) >> 2, wi = warp - 2;
+    const int r0 = rh * RPT;
     const int key = q4 * 32 + lane;
     const uint32_t lane_off = uint32_t(q4 * 32) << 16;
-    float m[16], mt[16], ls[16];
+    float m[RPT], mt[RPT], ls[RPT];
 #pragma unroll
-    for (int r = 0; r < 16; ++r) { m[r] = -INFINITY; mt[r] = -INFINITY; ls[r] = 0.f; }
+    for (int i = 0; i < RPT; ++i) { m[i] = -INFINITY; mt[i] = -INFINITY; ls[i] = 0.f; }
     for (int jj = 0; jj < n; ++jj) {
       const int sb = jj & 1;
       const uint32_t ph = (jj >> 1) & 1;
@@ -665,70 +674,76 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       const bool kvalid = blk * 128 + key <= pos;
       mbar_wait_ab(&bar_sf[sb], ph, err, &abort_s);
       tc_fence_after();
-      uint32_t v[16];
-      tmem_ld16(tmem + lane_off + sb * 16, v);
+      uint32_t v[RPT];
+      tmem_ldn<RPT>(tmem + lane_off + sb * 16 + r0, v);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_se[sb]);
-      float x[16];
+      float x[RPT];
       uint32_t over = 0;
 #pragma unroll
-      for (int r = 0; r < 16; ++r) {
-        x[r] = (r < G && kvalid && ((rmask >> r) & 1u)) ? __uint_as_float(v[r]) * qk_scale2 : -INFINITY;
-        mt[r] = fmaxf(mt[r], x[r]);
-        over |= (x[r] > m[r] + kDecLimit) ? (1u << r) : 0u;
+      for (int i = 0; i < RPT; ++i) {
+        const int r = r0 + i;
+        x[i] = (r < G && kvalid && ((rmask >> r) & 1u)) ? __uint_as_float(v[i]) * qk_scale2 : -INFINITY;
+        mt[i] = fmaxf(mt[i], x[i]);
+        over |= (x[i] > m[i] + kDecLimit) ? (1u << r) : 0u;
       }
       over = __reduce_or_sync(0xffffffffu, over);
-      if (lane == 0) flags[sb][q4] = over;
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-      const uint32_t E = flags[sb][0] | flags[sb][1] | flags[sb][2] | flags[sb][3];
-      float alpha[16];
+      if (lane == 0) flags[sb][wi] = over;
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      uint32_t E = 0;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) E |= flags[sb][w];
+      float alpha[RPT];
       bool need = false;
       if (E != 0) {                                // uniform: some row's reference must move
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-          if ((E >> r) & 1u) {
-            float mr = x[r];
+        for (int i = 0; i < RPT; ++i) {
+          if ((E >> (r0 + i)) & 1u) {
+            float mr = x[i];
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) mr = fmaxf(mr, __shfl_xor_sync(0xffffffffu, mr, o));
-            if (lane == 0) red[sb][q4][r] = mr;
+            if (lane == 0) red[sb][q4][r0 + i] = mr;
           }
         }
-        asm volatile("bar.sync 1, 128;" ::: "memory");
+        asm volatile("bar.sync 1, 256;" ::: "memory");
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-          alpha[r] = 1.0f;
+        for (int i = 0; i < RPT; ++i) {
+          const int r = r0 + i;
+          alpha[i] = 1.0f;
           if ((E >> r) & 1u) {
             const float bm = fmaxf(fmaxf(red[sb][0][r], red[sb][1][r]), fmaxf(red[sb][2][r], red[sb][3][r])) - kDecHead;
-            if (m[r] > -INFINITY) { alpha[r] = exp2f(m[r] - bm); need = true; }
-            m[r] = bm;
+            if (m[i] > -INFINITY) { alpha[i] = exp2f(m[i] - bm); need = true; }
+            m[i] = bm;
           }
         }
       }
       // P buffer sb is free once PV_{jj-2} is done (also bounds the pv parity below)
       mbar_wait_ab(&bar_pe[sb], ph ^ 1, err, &abort_s);
-      if (need) {                                  // uniform: every thread holds the same m
+      if (__any_sync(0xffffffffu, need)) {         // every thread of the warp holds the same m
         mbar_wait_ab(&bar_pv, (jj - 1) & 1, err, &abort_s);
         tc_fence_after();
-        uint32_t o[16];
-        tmem_ld16(tmem + lane_off + 32, o);
+        uint32_t o[RPT];
+        tmem_ldn<RPT>(tmem + lane_off + 32 + r0, o);
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-          o[r] = __float_as_uint(__uint_as_float(o[r]) * alpha[r]);
-          ls[r] *= alpha[r];
+        for (int i = 0; i < RPT; ++i) {
+          const float al = need ? alpha[i] : 1.0f;
+          o[i] = __float_as_uint(__uint_as_float(o[i]) * al);
+          ls[i] *= al;
         }
-        tmem_st16(tmem + lane_off + 32, o);
+        tmem_stn<RPT>(tmem + lane_off + 32 + r0, o);
         tc_fence_before();
       }
       // P -> three e4m3 terms, into row r, column `key` of each operand
       uint8_t* pbuf = smem + kDPOff + sb * 6144;
       const uint32_t kc = uint32_t(key >> 4), kb = uint32_t(key & 15);
 #pragma unroll
-      for (int r = 0; r < 16; r += 2) {
-        float p0 = fast_exp2(x[r] - (m[r] == -INFINITY ? 0.f : m[r]));
-        float p1 = fast_exp2(x[r + 1] - (m[r + 1] == -INFINITY ? 0.f : m[r + 1]));
-        ls[r] += p0;
-        ls[r + 1] += p1;
+      for (int i = 0; i < RPT; i += 2) {
+        const int r = r0 + i;
+        float p0 = fast_exp2(x[i] - (m[i] == -INFINITY ? 0.f : m[i]));
+        float p1 = fast_exp2(x[i + 1] - (m[i + 1] == -INFINITY ? 0.f : m[i + 1]));
+        ls[i] += p0;
+        ls[i + 1] += p1;
         const uint32_t o0 = swz_offset(uint32_t(r), kc, 128) + kb, o1 = swz_offset(uint32_t(r + 1), kc, 128) + kb;
 #pragma unroll
         for (int part = 0; part < 3; ++part) {
@@ -750,26 +765,27 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     // chunk result: O^T columns (rows) for this thread's d lane, and row state
     if (n > 0) mbar_wait_ab(&bar_done, 0, err, &abort_s);
     tc_fence_after();
-    uint32_t o[16];
-    tmem_ld16(tmem + lane_off + 32, o);
+    uint32_t o[RPT];
+    tmem_ldn<RPT>(tmem + lane_off + 32 + r0, o);
     const size_t base = (unit * max_chunks + c) * G;
 #pragma unroll
-    for (int r = 0; r < 16; ++r)
-      if (r < G) part_o[(base + r) * 128 + key] = __uint_as_float(o[r]);
+    for (int i = 0; i < RPT; ++i)
+      if (r0 + i < G) part_o[(base + r0 + i) * 128 + key] = __uint_as_float(o[i]);
 #pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      float sr = ls[r], mr = mt[r];
+    for (int i = 0; i < RPT; ++i) {
+      float sr = ls[i], mr = mt[i];
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) {
         sr += __shfl_xor_sync(0xffffffffu, sr, off);
         mr = fmaxf(mr, __shfl_xor_sync(0xffffffffu, mr, off));
       }
-      if (lane == 0) { red[0][q4][r] = sr; red[1][q4][r] = mr; }
+      if (lane == 0) { red[0][q4][r0 + i] = sr; red[1][q4][r0 + i] = mr; }
+      if (lane == 0 && q4 == 0) mrow[r0 + i] = m[i];
     }
-    asm volatile("bar.sync 1, 128;" ::: "memory");
+    asm volatile("bar.sync 1, 256;" ::: "memory");
     if (tid - 64 < G) {
       const int r = tid - 64;
-      part_s[base + r] = DecodePartial{m[r], red[0][0][r] + red[0][1][r] + red[0][2][r] + red[0][3][r],
+      part_s[base + r] = DecodePartial{mrow[r], red[0][0][r] + red[0][1][r] + red[0][2][r] + red[0][3][r],
                                        fmaxf(fmaxf(red[1][0][r], red[1][1][r]), fmaxf(red[1][2][r], red[1][3][r])),
                                        0.f};
     }
@@ -848,10 +864,11 @@ cudaError_t launch_decode(const AttnArgs& a, cudaStream_t stream, const char** w
                            CU_TENSOR_MAP_SWIZZLE_128B, why))
       return cudaErrorInvalidValue;
   }
-  cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecodeSmem);
+  auto kern = G <= 8 ? attn_decode_kernel<4> : attn_decode_kernel<8>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecodeSmem);
   if (e != cudaSuccess) return e;
   profile_mark(stream, 0);
-  attn_decode_kernel<<<a.T * a.Hkv * mc, 192, kDecodeSmem, stream>>>(
+  kern<<<a.T * a.Hkv * mc, kDecThreads, kDecodeSmem, stream>>>(
       tm_q, tm_k, tm_v, a.page_table, a.seq_lens, a.cu_q, a.topk, a.c_qk * kLog2e, a.B, a.T, a.Hq,
       a.Hkv, a.Hidx, a.topk_k, a.max_pages, a.num_pages, mc, part_o, part_s, n_chunks, a.err);
   profile_mark(stream, 1);

@@ -262,6 +262,46 @@ MSA_DEV void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "r"(taddr)
       : "memory");
 }
+// 8 / 4 consecutive 32-bit columns of this thread's TMEM lane, load + wait fused.
+MSA_DEV void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+      : "r"(taddr)
+      : "memory");
+}
+MSA_DEV void tmem_ld4(uint32_t taddr, uint32_t (&r)[4]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+      : "r"(taddr)
+      : "memory");
+}
+// Store 8 / 4 consecutive 32-bit columns to this thread's TMEM lane, then wait.
+MSA_DEV void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+      : "memory");
+}
+MSA_DEV void tmem_st4(uint32_t taddr, const uint32_t (&r)[4]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
+      : "memory");
+}
+// Column loads/stores of a compile-time width 4 or 8.
+template <int N>
+MSA_DEV void tmem_ldn(uint32_t taddr, uint32_t (&r)[N]) {
+  if constexpr (N == 8) tmem_ld8(taddr, r); else tmem_ld4(taddr, r);
+}
+template <int N>
+MSA_DEV void tmem_stn(uint32_t taddr, const uint32_t (&r)[N]) {
+  if constexpr (N == 8) tmem_st8(taddr, r); else tmem_st4(taddr, r);
+}
 // Store 64 consecutive 32-bit columns to this thread's TMEM lane, then wait.
 MSA_DEV void tmem_st64(uint32_t taddr, const uint32_t (&r)[64]) {
   asm volatile(
