@@ -255,12 +255,15 @@ index_score_decode_kernel(const __grid_constant__ CUtensorMap tm_q,
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_tempty[buf]);
+      // block maximum of each index head (columns past Hidx are padding)
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
-        float m = __uint_as_float(v[c]);
+        if (c < Hidx) {                                // uniform across the CTA
+          float m = __uint_as_float(v[c]);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        if (lane == 0 && c < Hidx) atomicMax(&sred[j][c], order_key(m));
+          for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+          if (lane == 0) atomicMax(&sred[j][c], order_key(m));
+        }
       }
     }
     asm volatile("bar.sync 1, 128;" ::: "memory");
