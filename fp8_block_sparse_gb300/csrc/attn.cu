@@ -282,7 +282,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       }
       const int ncol = !sel ? 0 : (blk < own ? 128 : pos - blk * 128 + 1);
       // S_X(j) done (and with it PV_X(j-1): O is settled and P may be rewritten)
-      if (!mbar_wait_ab(&bar_sf[X], j & 1, err, &abort_s)) break;
+      if (!mbar_wait_warp(&bar_sf[X], j & 1, err, &abort_s)) break;   // uniform: tcgen05 ops follow
       tc_fence_after();
       float x[128];
       {

@@ -17,14 +17,17 @@
 // part is 53% of the flops; duplicating it costs 1.5x the MMA work of one CTA
 // per token, and the two halves run as separate CTAs on different SMs).
 // Per 64-key chunk of the index list:
-//   gather   four producer warps copy the 64 kv rows (576 B each) with 16-byte
-//            cp.async into a K-major tile: four 128-byte swizzled regions plus
-//            one 64-byte swizzled region for the last 64 columns; invalid
-//            entries become zero rows (and are masked);
+//   gather   four warps copy the 64 kv rows (576 B each; a whole warp per
+//            row, 16-byte cp.async, indices loaded one chunk ahead) into a
+//            K-major tile: four 128-byte swizzled regions plus one 64-byte
+//            swizzled region for the last 64 columns; invalid entries become
+//            zero rows (and are masked);
 //   S = Q K^T  tcgen05 e4m3, M=128, N=64, K=576 (18 MMAs), double-buffered TMEM;
-//   V        the same warps widen this CTA's 256 V columns of the tile to
+//   V        four more warps widen this CTA's 256 V columns of the tile to
 //            f16 in place of layout (rows = keys, 16-byte loads, two 16-byte
-//            stores each, no transpose); PV reads it as an MN-major operand;
+//            stores each, no transpose) into a double-buffered image, while
+//            the gather warps fetch the next chunk; PV reads it as an MN-major
+//            operand;
 //   P        one thread per head row: online softmax with lazy rescale, P in
 //            f16 (e4m3 P costs ~2.5% relative error on flat rows);
 //   O += P V tcgen05 kind::f16, M=128, N=256, K=64, B (V) MN-major.
@@ -56,7 +59,9 @@ constexpr uint32_t kTP = 128, kTO = 256;
 constexpr uint32_t kIdescQK = idesc_f32(128, 64);
 constexpr uint32_t kIdescPV = idesc_f32(128, 256) | (1u << 16);   // B MN-major
 
-__global__ void __launch_bounds__(288, 1)
+constexpr int kMlaThreads = 416;   // MMA, 4 gather, 4 softmax, 4 widening warps
+
+__global__ void __launch_bounds__(kMlaThreads, 1)
 mla_prefill_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_constant__ CUtensorMap tm_q64,
                    const uint8_t* __restrict__ kv, const int32_t* __restrict__ indices,
                    const int32_t* __restrict__ topk_length, const float* __restrict__ sink,
@@ -144,7 +149,7 @@ mla_prefill_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_con
       }
     }
   } else if (warp <= 4) {
-    // ---------------- producers: gather chunk j, widen chunk j-1
+    // ---------------- gather warps: copy chunk j, then publish chunk j-1 once it has landed
     // Gather: producer warp pw copies rows 16*pw .. 16*pw+15 of the chunk, one
     // row at a time with all 32 lanes (576 bytes = 36 chunks of 16 bytes), so
     // every cp.async instruction reads contiguous bytes of one kv row.
@@ -189,34 +194,41 @@ mla_prefill_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_con
         fence_async_shared();
         asm volatile("bar.sync 2, 128;" ::: "memory");        // chunk jp has landed
         if (pt == 0) mbar_arrive(&bar_kf[sp]);
-        // V for this CTA's d_v half as f16, rows = keys: item = (key, 16 columns)
-        mbar_wait_ab(&bar_vte[sp], ((jp >> 1) & 1) ^ 1, err, &abort_s);   // PV(jp-2) done
-        const uint8_t* stage = smem + kKOff + sp * kKStage;
-        uint8_t* vimg = smem + kVTOff + sp * 32768;
-#pragma unroll 2
-        for (int x = pt; x < kChunkKeys * 16; x += 128) {
-          const int kr = x >> 4, g16 = x & 15;
-          const int d0 = hf * 256 + g16 * 16;                   // first of 16 columns
-          const uint4 v = *reinterpret_cast<const uint4*>(stage + (d0 >> 7) * 8192 +
-                                                          swz_offset(kr, (d0 & 127) >> 4, 128));
-          uint4 lo4, hi4;
-          lo4.x = e4m3x2_to_f16x2(uint16_t(v.x)); lo4.y = e4m3x2_to_f16x2(uint16_t(v.x >> 16));
-          lo4.z = e4m3x2_to_f16x2(uint16_t(v.y)); lo4.w = e4m3x2_to_f16x2(uint16_t(v.y >> 16));
-          hi4.x = e4m3x2_to_f16x2(uint16_t(v.z)); hi4.y = e4m3x2_to_f16x2(uint16_t(v.z >> 16));
-          hi4.z = e4m3x2_to_f16x2(uint16_t(v.w)); hi4.w = e4m3x2_to_f16x2(uint16_t(v.w >> 16));
-          const int dl = g16 * 16;                               // local column 0..255
-          uint8_t* blk = vimg + (dl >> 6) * 8192;                // 64 f16 columns per 128-byte row
-          const uint32_t c0 = uint32_t(dl & 63) >> 3;
-          *reinterpret_cast<uint4*>(blk + swz_offset(kr, c0, 128)) = lo4;
-          *reinterpret_cast<uint4*>(blk + swz_offset(kr, c0 + 1, 128)) = hi4;
-        }
-        fence_async_shared();
-        __syncwarp();
-        if (lane == 0) { mbar_arrive(&bar_vtf[sp]); mbar_arrive(&bar_ke[sp]); }
       }
     }
+  } else if (warp >= 9) {
+    // ---------------- widening warps: V of chunk jp to f16 once it has landed
+    const int ct = tid - 288;
+    for (int jp = 0; jp < nch; ++jp) {
+      const int sp = jp & 1;
+      mbar_wait_ab(&bar_kf[sp], (jp >> 1) & 1, err, &abort_s);
+      // V for this CTA's d_v half as f16, rows = keys: item = (key, 16 columns)
+      mbar_wait_ab(&bar_vte[sp], ((jp >> 1) & 1) ^ 1, err, &abort_s);   // PV(jp-2) done
+      const uint8_t* stage = smem + kKOff + sp * kKStage;
+      uint8_t* vimg = smem + kVTOff + sp * 32768;
+#pragma unroll 2
+      for (int x = ct; x < kChunkKeys * 16; x += 128) {
+        const int kr = x >> 4, g16 = x & 15;
+        const int d0 = hf * 256 + g16 * 16;                   // first of 16 columns
+        const uint4 v = *reinterpret_cast<const uint4*>(stage + (d0 >> 7) * 8192 +
+                                                        swz_offset(kr, (d0 & 127) >> 4, 128));
+        uint4 lo4, hi4;
+        lo4.x = e4m3x2_to_f16x2(uint16_t(v.x)); lo4.y = e4m3x2_to_f16x2(uint16_t(v.x >> 16));
+        lo4.z = e4m3x2_to_f16x2(uint16_t(v.y)); lo4.w = e4m3x2_to_f16x2(uint16_t(v.y >> 16));
+        hi4.x = e4m3x2_to_f16x2(uint16_t(v.z)); hi4.y = e4m3x2_to_f16x2(uint16_t(v.z >> 16));
+        hi4.z = e4m3x2_to_f16x2(uint16_t(v.w)); hi4.w = e4m3x2_to_f16x2(uint16_t(v.w >> 16));
+        const int dl = g16 * 16;                               // local column 0..255
+        uint8_t* blk = vimg + (dl >> 6) * 8192;                // 64 f16 columns per 128-byte row
+        const uint32_t c0 = uint32_t(dl & 63) >> 3;
+        *reinterpret_cast<uint4*>(blk + swz_offset(kr, c0, 128)) = lo4;
+        *reinterpret_cast<uint4*>(blk + swz_offset(kr, c0 + 1, 128)) = hi4;
+      }
+      fence_async_shared();
+      __syncwarp();
+      if (lane == 0) { mbar_arrive(&bar_vtf[sp]); mbar_arrive(&bar_ke[sp]); }
+    }
   } else {
-    // ---------------- softmax: thread = head row (TMEM lane)
+    // ---------------- softmax (warps 5-8): thread = head row (TMEM lane)
     const int q4 = warp & 3;
     const int row = q4 * 32 + lane;
     const uint32_t lane_off = uint32_t(q4 * 32) << 16;
@@ -345,7 +357,7 @@ cudaError_t launch_sparse_mla(const MlaArgs& a, cudaStream_t stream, const char*
   cudaError_t e = cudaFuncSetAttribute(mla_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMlaSmem);
   if (e != cudaSuccess) return e;
   profile_mark(stream, 0);
-  mla_prefill_kernel<<<a.T * 2, 288, kMlaSmem, stream>>>(
+  mla_prefill_kernel<<<a.T * 2, kMlaThreads, kMlaSmem, stream>>>(
       tm_q128, tm_q64, a.kv, a.indices, a.topk_length, a.sink, a.c_qk * kLog2e, a.c_sink * kLog2e,
       a.v_scale, a.T, a.S_kv, a.topk, a.out, a.max_logits, a.lse, a.err);
   profile_mark(stream, 1);
