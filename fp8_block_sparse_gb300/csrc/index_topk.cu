@@ -311,15 +311,30 @@ topk_select_kernel(const float* __restrict__ scores, const int32_t* __restrict__
     const int id = r * 32 + lane;
     key[r] = id < own ? order_key(__ldg(s + id)) : 0u;   // 0 sorts below every score
   }
-  // largest tau with #{key >= tau} >= kp: the kp-th largest key
-  uint32_t tau = 0;
-  for (int bit = 31; bit >= 0; --bit) {
+  // largest tau with #{key >= tau} >= kp: the kp-th largest key. The bits
+  // every candidate shares are the same in tau (all candidates lie on one
+  // side of each such bit), so the search starts below them; and once
+  // exactly kp keys reach tau the selected set cannot change any more.
+  uint32_t kand = 0xFFFFFFFFu, kor = 0u;
+#pragma unroll
+  for (int r = 0; r < NPL; ++r) {
+    if (r * 32 + lane < own) { kand &= key[r]; kor |= key[r]; }
+  }
+  kand = __reduce_and_sync(0xffffffffu, kand);
+  kor = __reduce_or_sync(0xffffffffu, kor);
+  const uint32_t diff = kand ^ kor;
+  const int top = diff ? 31 - __clz(diff) : -1;            // highest bit that differs
+  uint32_t tau = top < 0 ? kand : (top == 31 ? 0u : (kand & ~((2u << top) - 1u)));
+  for (int bit = top; bit >= 0; --bit) {
     const uint32_t tr = tau | (1u << bit);
     int cnt = 0;
 #pragma unroll
     for (int r = 0; r < NPL; ++r) cnt += key[r] >= tr;
     cnt = __reduce_add_sync(0xffffffffu, cnt);
-    if (cnt >= kp) tau = tr;
+    if (cnt >= kp) {
+      tau = tr;
+      if (cnt == kp) break;                                 // uniform: cnt is warp-wide
+    }
   }
   int gt = 0;
 #pragma unroll
