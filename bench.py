@@ -372,6 +372,23 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
 
 
+def world_max(ms: float, world: int, device=None) -> float:
+    """Largest per-rank duration over the job (the slowest replica sets the
+    job's time); the process group must be initialised when world > 1."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, world: int, steps: int, job_ms: float) -> float:
+    """Whole-job throughput: every replica processes its own units each step."""
+    return units_per_rank * world * steps / (job_ms / 1e3)
+
+
 def reference_arm(args):
     rank, _, world = dist_env()
     if rank != 0:
@@ -406,7 +423,6 @@ def reference_arm(args):
 
 def _e2e(msa, st, args, world, dev, h2d, d2h, barrier, T):
     import torch
-    import torch.distributed as dist
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for _ in range(args.steps):
@@ -418,12 +434,8 @@ def _e2e(msa, st, args, world, dev, h2d, d2h, barrier, T):
         st["ml_host"].copy_(st["ml"], non_blocking=True)
     e1.record()
     barrier()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
-    e2e = {"value": T * world * args.steps / (e2e_ms / 1e3), "unit": UNIT,
+    e2e_ms = world_max(e0.elapsed_time(e1), world, dev)
+    e2e = {"value": job_throughput(T, world, args.steps, e2e_ms), "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
     return e2e
@@ -490,11 +502,7 @@ def native_arm(args):
     barrier()
     clk = clocks.stop()
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    total_ms = sum(step_ms)
-    if world > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = world_max(sum(step_ms), world, dev)
     quant_ms = statistics.mean(c[0].elapsed_time(c[1]) for c in cuts)
     index_ms = statistics.mean(c[1].elapsed_time(c[2]) for c in cuts)
     attn_call_ms = statistics.mean(c[2].elapsed_time(c[3]) for c in cuts)
@@ -502,7 +510,7 @@ def native_arm(args):
     msa.check_errors()
 
     T = st["w"].T
-    value = T * world * args.steps / (total_ms / 1e3)
+    value = job_throughput(T, world, args.steps, total_ms)
     n_keys = selected_keys(st)
     flops = alg_flops(st, n_keys)
     exe = executed_flops(st)
