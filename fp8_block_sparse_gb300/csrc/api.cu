@@ -222,7 +222,7 @@ msa_status msa_index_topk(const uint8_t* idx_q, const uint8_t* idx_k_cache,
   const char* fn = "msa_index_topk";
   if (B < 1 || T < 0 || Hidx < 1 || num_pages < 1 || max_pages < 1)
     return fail(MSA_ERR_INVALID_ARG, std::string(fn) + ": bad B/T/Hidx/num_pages/max_pages");
-  if (max_q_len < 1 || (T > 0 && max_q_len > T))
+  if (T > 0 && (max_q_len < 1 || max_q_len > T))
     return fail(MSA_ERR_INVALID_ARG, std::string(fn) + ": max_q_len must be in [1, T]");
   if (D != 64 && D != 128)
     return fail(MSA_ERR_UNSUPPORTED, std::string(fn) + ": index head dim must be 64 or 128");
@@ -280,7 +280,7 @@ msa_status msa_sparse_attn_fwd(const uint8_t* q, const uint8_t* k_cache, const u
   const char* fn = "msa_sparse_attn_fwd";
   if (B < 1 || T < 0 || Hq < 1 || Hkv < 1 || Hidx < 1 || num_pages < 1 || max_pages < 1)
     return fail(MSA_ERR_INVALID_ARG, std::string(fn) + ": bad sizes");
-  if (max_q_len < 1 || (T > 0 && max_q_len > T))
+  if (T > 0 && (max_q_len < 1 || max_q_len > T))
     return fail(MSA_ERR_INVALID_ARG, std::string(fn) + ": max_q_len must be in [1, T]");
   if (Hq % Hkv != 0 || Hq % Hidx != 0)
     return fail(MSA_ERR_INVALID_ARG, std::string(fn) + ": Hq must be a multiple of Hkv and of Hidx");

@@ -39,6 +39,9 @@
  *   rows cu_q[b] .. cu_q[b+1]-1 of the query tensors. Prefill of one
  *   sequence: B = 1, cu_q = {0, T}, seq_lens = {T}. Decode: q_len_b = 1.
  *   max_q_len is the host's bound on q_len_b (1 selects the decode kernels).
+ *   A sequence may have q_len_b = 0. With T = 0 every entry point returns
+ *   MSA_OK at once, after checking its scalar arguments, without reading
+ *   any pointer (max_q_len is not checked then).
  *   page_table[b * max_pages + j] is the physical page of logical block j.
  *
  * Sources: the four web pages this method is described on --

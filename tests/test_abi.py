@@ -98,3 +98,19 @@ def test_mla_validation(lib):
     assert f(576, 256, 128, 2048) == 2          # d_v must be 512
     assert f(512, 512, 128, 2048) == 2          # d_qk must be 576
     assert f(576, 512, 64, 2048) == 2           # 128 heads
+
+
+def test_empty_batches_return_ok_without_touching_pointers(lib):
+    # T = 0: scalar checks only, no pointer is read and no CUDA work is issued
+    null = None
+    assert lib.msa_index_topk(null, null, null, null, null, 1, 0, 0, 4, 128, 64, 1, 1,
+                              null, null, 0, null) == 0
+    assert lib.msa_sparse_attn_fwd(null, null, null, null, null, null, null, null, 0.1, None, None, None,
+                                   1, 0, 0, 16, 2, 4, 128, 64, 1, 1, null, null, null, null, 0, null) == 0
+    assert lib.msa_sparse_mla_fwd(null, null, null, null, null, 0.1, None, None, 0, 128, 64, 576, 512, 2048,
+                                  null, null, null, null) == 0
+    # bad scalars are still rejected when T = 0
+    assert lib.msa_index_topk(null, null, null, null, null, 1, 0, 0, 4, 96, 64, 1, 1,
+                              null, null, 0, null) == 2                      # d_idx 96
+    assert lib.msa_sparse_attn_fwd(null, null, null, null, null, null, null, null, -1.0, None, None, None,
+                                   1, 0, 0, 16, 2, 4, 128, 64, 1, 1, null, null, null, null, 0, null) == 1
