@@ -553,9 +553,37 @@ def native_arm(args):
             torch.cuda.synchronize()
             d_ms.append(a.elapsed_time(b))
         msa.check_errors()
+        # the same step captured once as a CUDA graph (quantise -> index top-k
+        # -> attention chained without host work between launches) and replayed
+        msa.profile_enable(False)
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            run_path(msa, ds)
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            run_path(msa, ds)
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+        g_ms = []
+        for k in range(args.steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            graph.replay()
+            b.record()
+            torch.cuda.synchronize()
+            g_ms.append(a.elapsed_time(b))
+        msa.check_errors()
+        del graph
+        msa.profile_enable(True)
         total_b, kv_b, union = decode_bytes(ds)
         step_ms_d = statistics.mean(d_ms)
         kern_d = statistics.mean(d_kern)
+        step_ms_g = statistics.mean(g_ms)
         decode = {"workload": "decode", "batch": ds["w"].T, "ms_per_step": step_ms_d,
                   "tokens_per_s": ds["w"].T / (step_ms_d / 1e3),
                   "hbm_gbs": total_b / (step_ms_d / 1e3) / 1e9,
@@ -565,7 +593,9 @@ def native_arm(args):
                                   "frac_of_hbm": kv_b / (kern_d / 1e3) / 1e9 / pk["hbm_gbs"],
                                   "traffic": traffic_for("attn.cu", "attn_decode_kernel_decode_traffic.md")},
                   "algorithmic_bytes_per_step": total_b, "kv_union_blocks": union,
-                  "peak_hbm_gbs": pk["hbm_gbs"], "peak_basis": pk["source"]}
+                  "peak_hbm_gbs": pk["hbm_gbs"], "peak_basis": pk["source"],
+                  "graph_replay": {"ms_per_step": step_ms_g, "tokens_per_s": ds["w"].T / (step_ms_g / 1e3),
+                                   "hbm_gbs": total_b / (step_ms_g / 1e3) / 1e9}}
         del ds
 
     mla = None
