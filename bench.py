@@ -326,6 +326,50 @@ def mla_measure(msa, wl, dev, steps, flush, pk):
             "peak_basis": f"{pk['source']} bf16 burst x2"}
 
 
+def kv_store_measure(msa, w, dev, steps, flush, pk):
+    """The quantised KV-cache store of a workload's new tokens (K, V and index
+    K of every query row into the paged e4m3 pools), one launch per step."""
+    import numpy as np
+    import torch
+    c = w.cfg
+    T = w.T
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    g = torch.Generator(device="cpu").manual_seed(7)
+    k = (torch.randn((T, c.Hkv, c.D), generator=g) * 2).to(torch.bfloat16).to(dev)
+    v = (torch.randn((T, c.Hkv, c.D), generator=g) * 2).to(torch.bfloat16).to(dev)
+    ik = (torch.randn((T, c.d_idx), generator=g) * 2).to(torch.bfloat16).to(dev)
+    kc = torch.zeros((w.num_pages, c.Hkv, 128, c.D), dtype=torch.uint8, device=dev)
+    vc, ic = torch.zeros_like(kc), torch.zeros((w.num_pages, 128, c.d_idx), dtype=torch.uint8, device=dev)
+    pt, sl, cu = t(w.page_table), t(w.seq_lens), t(w.cu_q)
+
+    def step():
+        msa.kv_store_fp8(pt, sl, cu, kc, vc, ic, k=k, v=v, idx_k=ik,
+                         k_scale=w.scales["k"], v_scale=w.scales["v"], idx_k_scale=w.scales["idx_k"])
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    ms = []
+    for _ in range(steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        step()
+        b.record()
+        torch.cuda.synchronize()
+        ms.append(a.elapsed_time(b))
+    msa.check_errors()
+    # algorithmic bytes: 2 B read + 1 B written per element, plus the batch description
+    elems = T * (2 * c.Hkv * c.D + c.d_idx)
+    nbytes = 3 * elems + 4 * (w.page_table.size + w.seq_lens.size + w.cu_q.size)
+    m = statistics.mean(ms)
+    del kc, vc, ic, k, v, ik
+    return {"workload": c.name, "tokens": T, "kernel": "kv_store_kernel", "ms": m,
+            "gbs": nbytes / (m / 1e3) / 1e9, "frac_of_hbm": nbytes / (m / 1e3) / 1e9 / pk["hbm_gbs"],
+            "algorithmic_bytes": nbytes, "peak_basis": pk["source"]}
+
+
 # ----------------------------------------------------------------- CPU oracle
 def oracle_codes(w):
     from oracle import quant as oq
@@ -532,7 +576,9 @@ def native_arm(args):
     if not args.no_e2e:
         e2e = _e2e(msa, st, args, world, dev, h2d, d2h, barrier, T)
 
-    # ---- paged decode workload: HBM GB/s
+    # ---- the quantised KV-cache store of this workload's new tokens
+    kv_store = [kv_store_measure(msa, st["w"], dev, args.steps, flush, pk)]
+
     # ---- paged decode workload: HBM GB/s
     decode = None
     if not args.no_decode:
@@ -580,6 +626,7 @@ def native_arm(args):
         msa.check_errors()
         del graph
         msa.profile_enable(True)
+        kv_store.append(kv_store_measure(msa, ds["w"], dev, args.steps, flush, pk))
         total_b, kv_b, union = decode_bytes(ds)
         step_ms_d = statistics.mean(d_ms)
         kern_d = statistics.mean(d_kern)
@@ -626,6 +673,7 @@ def native_arm(args):
                              "attention_kernel": kern_ms},
             "decode": decode,
             "mla": mla,
+            "kv_store": kv_store,
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": LAUNCHES_PREFILL * args.steps,

@@ -46,6 +46,8 @@ _SIGNATURES = {
     "msa_profile_enable": ([_I], _I),
     "msa_profile_last_ms": ([_FP], _I),
     "msa_quant_fp8": ([_P, _I, _I64, _I64, _I64, _P, _I, _I64, _FP, _P], _I),
+    "msa_kv_store_fp8": ([_P, _P, _P, _I, _I64, _I64, _I64, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
+                          _FP, _FP, _FP, _P, _P, _P, _P], _I),
     "msa_index_topk_workspace_size": ([_I, _I, _I], _SZ),
     "msa_index_topk": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P], _I),
     "msa_index_topk_noalloc": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P], _I),
@@ -137,6 +139,64 @@ def quant_fp8(x: torch.Tensor, scale: Optional[float] = None, out: Optional[torc
                              rows, cols, x2.stride(0) if rows else cols, _ptr(o2), MSA_E4M3,
                              o2.stride(0) if rows else cols, _scale(scale), _stream(stream)))
     return out
+
+
+def _token_rows(x: Optional[torch.Tensor], name: str, inner: int):
+    """Token stride of x, whose per-token block of `inner` elements is contiguous."""
+    if x is None:
+        return 0
+    if not x.is_cuda or x.dtype not in (torch.bfloat16, torch.float16):
+        raise MsaError(1, f"{name} must be a bf16 or fp16 CUDA tensor")
+    want, acc = [], 1
+    for n in reversed(x.shape[1:]):
+        want.insert(0, acc)
+        acc *= n
+    if acc != inner or any(n > 1 and st != w for n, st, w in zip(x.shape[1:], x.stride()[1:], want)):
+        raise MsaError(1, f"{name} must be [T, ...] with {inner} contiguous elements per token")
+    return x.stride(0) if x.shape[0] > 1 else inner
+
+
+def kv_store_fp8(page_table: torch.Tensor, seq_lens: torch.Tensor, cu_q: torch.Tensor,
+                 k_cache: Optional[torch.Tensor] = None, v_cache: Optional[torch.Tensor] = None,
+                 idx_k_cache: Optional[torch.Tensor] = None, k: Optional[torch.Tensor] = None,
+                 v: Optional[torch.Tensor] = None, idx_k: Optional[torch.Tensor] = None,
+                 k_scale: Optional[float] = None, v_scale: Optional[float] = None,
+                 idx_k_scale: Optional[float] = None, stream=None) -> None:
+    """Quantise new K [T, Hkv, D], V and index K [T, d_idx] into the paged e4m3
+    caches in place, at the slots the batch description gives."""
+    lib = load()
+    given = [x for x in (k, v, idx_k) if x is not None]
+    if not given:
+        return
+    dt = given[0].dtype
+    if any(x.dtype != dt for x in given):
+        raise MsaError(1, "k, v and idx_k must share one dtype")
+    for t, n in ((page_table, "page_table"), (seq_lens, "seq_lens"), (cu_q, "cu_q")):
+        _dev(t, n, torch.int32)
+    for c, n in ((k_cache, "k_cache"), (v_cache, "v_cache"), (idx_k_cache, "idx_k_cache")):
+        if c is not None:
+            _dev(c, n, torch.uint8)
+    kv = k if k is not None else v
+    T = given[0].shape[0]
+    Hkv, D = (kv.shape[1], kv.shape[2]) if kv is not None else (0, 16)
+    d_idx = idx_k.shape[1] if idx_k is not None else 16
+    parts = [(x, c, n, shape) for x, c, n, shape in
+             ((k, k_cache, "k_cache", (Hkv, 128, D)), (v, v_cache, "v_cache", (Hkv, 128, D)),
+              (idx_k, idx_k_cache, "idx_k_cache", (128, d_idx))) if x is not None]
+    if any(c is None for _, c, _, _ in parts):
+        raise MsaError(1, "every given input needs its cache")
+    cache = parts[0][1]
+    for _, c, n, shape in parts:
+        if tuple(c.shape[1:]) != shape or c.shape[0] != cache.shape[0]:
+            raise MsaError(1, f"{n} must be [num_pages, {', '.join(map(str, shape))}], got {tuple(c.shape)}")
+    B, max_pages = page_table.shape
+    _check(lib.msa_kv_store_fp8(_ptr(k), _ptr(v), _ptr(idx_k),
+                                MSA_BF16 if dt == torch.bfloat16 else MSA_FP16,
+                                _token_rows(k, "k", Hkv * D), _token_rows(v, "v", Hkv * D),
+                                _token_rows(idx_k, "idx_k", d_idx), _ptr(page_table), _ptr(seq_lens),
+                                _ptr(cu_q), B, T, max_pages, cache.shape[0], Hkv, D, d_idx,
+                                _scale(k_scale), _scale(v_scale), _scale(idx_k_scale),
+                                _ptr(k_cache), _ptr(v_cache), _ptr(idx_k_cache), _stream(stream)))
 
 
 def index_topk_workspace_size(T: int, Hidx: int, max_pages: int) -> int:

@@ -209,6 +209,75 @@ msa_status msa_quant_fp8(const void* x, msa_dtype x_dtype, int64_t rows, int64_t
   return MSA_OK;
 }
 
+msa_status msa_kv_store_fp8(const void* k, const void* v, const void* idx_k, msa_dtype in_dtype,
+                            int64_t k_token_stride, int64_t v_token_stride,
+                            int64_t idx_k_token_stride, const int32_t* page_table,
+                            const int32_t* seq_lens, const int32_t* cu_q, int B, int T,
+                            int max_pages, int num_pages, int Hkv, int D, int d_idx,
+                            const float* k_scale, const float* v_scale, const float* idx_k_scale,
+                            void* k_cache, void* v_cache, void* idx_k_cache, msa_stream_t stream) {
+  const char* fn = "msa_kv_store_fp8";
+  if (in_dtype != MSA_BF16 && in_dtype != MSA_FP16)
+    return fail(MSA_ERR_INVALID_ARG, std::string(fn) + ": in_dtype must be MSA_BF16 or MSA_FP16");
+  if (B < 1 || T < 0 || max_pages < 1 || num_pages < 1)
+    return fail(MSA_ERR_INVALID_ARG, std::string(fn) + ": need B >= 1, T >= 0, max_pages >= 1, num_pages >= 1");
+  const bool has_kv = k != nullptr || v != nullptr;
+  if (has_kv && (Hkv < 1 || D < 16 || D % 16 != 0 || int64_t(Hkv) * D > (1 << 20)))
+    return fail(MSA_ERR_INVALID_ARG, std::string(fn) + ": need Hkv >= 1 and D a positive multiple of 16");
+  if (idx_k != nullptr && (d_idx < 16 || d_idx % 16 != 0 || d_idx > (1 << 20)))
+    return fail(MSA_ERR_INVALID_ARG, std::string(fn) + ": d_idx must be a positive multiple of 16");
+  float ks = 1.0f, vs = 1.0f, is = 1.0f;
+  if (!read_scale(k_scale, &ks, "msa_kv_store_fp8: k_scale") ||
+      !read_scale(v_scale, &vs, "msa_kv_store_fp8: v_scale") ||
+      !read_scale(idx_k_scale, &is, "msa_kv_store_fp8: idx_k_scale"))
+    return MSA_ERR_INVALID_ARG;
+  if (T == 0 || (!has_kv && idx_k == nullptr)) return MSA_OK;
+  if (page_table == nullptr || seq_lens == nullptr || cu_q == nullptr)
+    return fail(MSA_ERR_INVALID_ARG, std::string(fn) + ": null batch description");
+  const struct { const void* x; void* cache; int64_t stride, row; const char* name; } parts[3] = {
+      {k, k_cache, k_token_stride, int64_t(Hkv) * D, "k"},
+      {v, v_cache, v_token_stride, int64_t(Hkv) * D, "v"},
+      {idx_k, idx_k_cache, idx_k_token_stride, int64_t(d_idx), "idx_k"}};
+  for (const auto& p : parts) {
+    if (p.x == nullptr) continue;
+    if (p.cache == nullptr)
+      return fail(MSA_ERR_INVALID_ARG, std::string(fn) + ": " + p.name + " given without its cache");
+    if (p.stride < p.row || p.stride % 8 != 0)
+      return fail(MSA_ERR_INVALID_ARG, std::string(fn) + ": " + p.name +
+                                           " token stride must be >= its row and a multiple of 8");
+    if (!aligned(p.x, 16) || !aligned(p.cache, 16))
+      return fail(MSA_ERR_INVALID_ARG, std::string(fn) + ": " + p.name + " and its cache must be 16-byte aligned");
+  }
+  KvStoreArgs a;
+  a.k = static_cast<const uint16_t*>(k);
+  a.v = static_cast<const uint16_t*>(v);
+  a.idx_k = static_cast<const uint16_t*>(idx_k);
+  a.k_stride = k_token_stride;
+  a.v_stride = v_token_stride;
+  a.idx_stride = idx_k_token_stride;
+  a.page_table = page_table;
+  a.seq_lens = seq_lens;
+  a.cu_q = cu_q;
+  a.B = B;
+  a.T = T;
+  a.max_pages = max_pages;
+  a.num_pages = num_pages;
+  a.Hkv = has_kv ? Hkv : 0;
+  a.D = has_kv ? D : 16;
+  a.d_idx = idx_k ? d_idx : 16;
+  a.k_sinv = k_scale ? 1.0f / ks : 1.0f;
+  a.v_sinv = v_scale ? 1.0f / vs : 1.0f;
+  a.i_sinv = idx_k_scale ? 1.0f / is : 1.0f;
+  a.k_cache = static_cast<uint8_t*>(k_cache);
+  a.v_cache = static_cast<uint8_t*>(v_cache);
+  a.idx_cache = static_cast<uint8_t*>(idx_k_cache);
+  a.err = device_error_word();
+  if (a.err == nullptr) return fail(MSA_ERR_CUDA, std::string(fn) + ": no device error word");
+  cudaError_t e = launch_kv_store(a, in_dtype == MSA_BF16, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  return MSA_OK;
+}
+
 size_t msa_index_topk_workspace_size(int T, int Hidx, int max_pages) {
   if (T < 0 || Hidx < 0 || max_pages < 0) return 0;
   return index_workspace_bytes(T, Hidx, max_pages);

@@ -37,6 +37,24 @@ void profile_mark(cudaStream_t stream, int which);
 cudaError_t launch_quant(const void* x, bool bf16, int64_t rows, int64_t cols, int64_t x_stride,
                          uint8_t* out, int64_t out_stride, float s_inv, cudaStream_t stream);
 
+// The quantised KV-cache store (before the path). Token strides in elements.
+struct KvStoreArgs {
+  const uint16_t* k;       // [T][Hkv][D] or null
+  const uint16_t* v;       // [T][Hkv][D] or null
+  const uint16_t* idx_k;   // [T][d_idx] or null
+  int64_t k_stride, v_stride, idx_stride;
+  const int32_t* page_table;
+  const int32_t* seq_lens;
+  const int32_t* cu_q;
+  int B, T, max_pages, num_pages, Hkv, D, d_idx;
+  float k_sinv, v_sinv, i_sinv;
+  uint8_t* k_cache;        // [num_pages][Hkv][128][D]
+  uint8_t* v_cache;
+  uint8_t* idx_cache;      // [num_pages][128][d_idx]
+  unsigned* err;
+};
+cudaError_t launch_kv_store(const KvStoreArgs& a, bool bf16, cudaStream_t stream);
+
 // Step (b). Scores go to `scores` [Hidx][T][max_pages] fp32 (workspace).
 struct IndexArgs {
   const uint8_t* idx_q;

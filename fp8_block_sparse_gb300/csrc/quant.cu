@@ -1,8 +1,10 @@
-// quant.cu -- step (a): per-tensor e4m3 quantisation, out = e4m3(fp32(x) * s_inv).
+// quant.cu -- step (a): per-tensor e4m3 quantisation, out = e4m3(fp32(x) * s_inv),
+// and the quantised KV-cache store that feeds the path with the same rule.
 //
 // sglang PR 25460 page, key source excerpt of fp8_quantize (widen to fp32,
 // multiply by a host-side scale_inv, cast to fp8); sglang PR 30971 page,
-// implementation step 3 (_quant_q_fp8 on q and idx_q).
+// implementation step 3 (_quant_q_fp8 on q and idx_q) and step 4 (the sparse KV
+// pool's K / V / index-K stores with per-tensor scales, None = unit scale).
 //
 // Pure streaming work (2 bytes in, 1 byte out per element), so the kernel is
 // built for HBM: each thread moves 16 elements per step as two 16-byte loads
@@ -135,7 +137,111 @@ __global__ void __launch_bounds__(256) quant_scalar_kernel(const uint16_t* __res
   }
 }
 
+// The quantised KV-cache store. One block owns `tpb` consecutive new tokens:
+// their threads first resolve each token's (page, slot) from the batch
+// description into shared memory, then the block walks the tokens' 16-element
+// chunks (K heads, V heads, index K), four chunks in flight per thread. Each
+// chunk is two 16-byte streaming loads and one 16-byte store; a (page, head,
+// slot) row of D codes is written by D/16 neighbouring threads.
+template <bool BF16>
+__global__ void __launch_bounds__(256) kv_store_kernel(KvStoreArgs a, int tpb) {
+  __shared__ int s_page[256];
+  __shared__ int s_slot[256];
+  const int t0 = blockIdx.x * tpb;
+  const int nt = min(tpb, a.T - t0);
+  if (int(threadIdx.x) < nt) {
+    const int t = t0 + threadIdx.x;
+    int lo = 0, hi = a.B - 1;                 // last sequence whose first row is <= t
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (__ldg(a.cu_q + mid) <= t) lo = mid; else hi = mid - 1;
+    }
+    const int q0 = __ldg(a.cu_q + lo), qlen = __ldg(a.cu_q + lo + 1) - q0;
+    const int pos = __ldg(a.seq_lens + lo) - qlen + (t - q0);
+    int page = -1;
+    if (pos >= 0 && t - q0 < qlen && (pos >> 7) < a.max_pages)
+      page = __ldg(a.page_table + int64_t(lo) * a.max_pages + (pos >> 7));
+    if (page < 0 || page >= a.num_pages) {
+      atomicOr(a.err, MSA_DEVERR_DATA);
+      page = -1;
+    }
+    s_page[threadIdx.x] = page;
+    s_slot[threadIdx.x] = pos & 127;
+  }
+  __syncthreads();
+  const int cd = a.D / 16;
+  const int nk = a.k ? a.Hkv * cd : 0, nv = a.v ? a.Hkv * cd : 0, ni = a.idx_k ? a.d_idx / 16 : 0;
+  const int cpt = nk + nv + ni;
+  const int total = nt * cpt;
+  constexpr int U = 4;
+  for (int c0 = threadIdx.x; c0 < total; c0 += U * 256) {
+    const uint4* src[U];
+    uint4* dst[U];
+    float sinv[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int c = c0 + u * 256;
+      dst[u] = nullptr;
+      src[u] = nullptr;
+      sinv[u] = 1.0f;
+      if (c >= total) continue;
+      const int tl = c / cpt;
+      int r = c - tl * cpt;
+      const int page = s_page[tl];
+      if (page < 0) continue;
+      const int64_t t = t0 + tl;
+      const int slot = s_slot[tl];
+      if (r < nk + nv) {
+        const bool is_k = r < nk;
+        if (!is_k) r -= nk;
+        const int h = r / cd, cc = r - h * cd;
+        const uint16_t* x = is_k ? a.k + t * a.k_stride : a.v + t * a.v_stride;
+        uint8_t* cache = is_k ? a.k_cache : a.v_cache;
+        src[u] = reinterpret_cast<const uint4*>(x + r * 16);
+        dst[u] = reinterpret_cast<uint4*>(cache + ((int64_t(page) * a.Hkv + h) * 128 + slot) * a.D +
+                                          cc * 16);
+        sinv[u] = is_k ? a.k_sinv : a.v_sinv;
+      } else {
+        r -= nk + nv;
+        src[u] = reinterpret_cast<const uint4*>(a.idx_k + t * a.idx_stride + r * 16);
+        dst[u] = reinterpret_cast<uint4*>(a.idx_cache + (int64_t(page) * 128 + slot) * a.d_idx + r * 16);
+        sinv[u] = a.i_sinv;
+      }
+    }
+    uint4 lo[U], hi[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (dst[u]) {
+        lo[u] = __ldcs(src[u]);
+        hi[u] = __ldcs(src[u] + 1);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (dst[u]) *dst[u] = quant16<BF16>(lo[u], hi[u], sinv[u]);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_kv_store(const KvStoreArgs& a, bool bf16, cudaStream_t stream) {
+  if (a.T == 0) return cudaSuccess;
+  const int cd = a.D / 16;
+  const int cpt = (a.k ? a.Hkv * cd : 0) + (a.v ? a.Hkv * cd : 0) + (a.idx_k ? a.d_idx / 16 : 0);
+  if (cpt == 0) return cudaSuccess;
+  // about 2048 chunks (8 per thread) per block, but at least two blocks per
+  // SM when the batch allows it
+  int tpb = 2048 / cpt;
+  const int spread = (a.T + 2 * num_sms() - 1) / (2 * num_sms());
+  tpb = tpb < spread ? tpb : spread;
+  tpb = tpb < 1 ? 1 : (tpb > 256 ? 256 : tpb);
+  const int grid = (a.T + tpb - 1) / tpb;
+  if (bf16)
+    kv_store_kernel<true><<<grid, 256, 0, stream>>>(a, tpb);
+  else
+    kv_store_kernel<false><<<grid, 256, 0, stream>>>(a, tpb);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_quant(const void* x, bool bf16, int64_t rows, int64_t cols, int64_t x_stride,
                          uint8_t* out, int64_t out_stride, float s_inv, cudaStream_t stream) {

@@ -2,7 +2,8 @@
  * msa.h -- C ABI of libmsa.so: FP8 (e4m3) top-k block-sparse attention on
  * GB300 (sm_103a).
  *
- * The library computes the three steps of the sparse-attention hot path:
+ * The library computes the three steps of the sparse-attention hot path,
+ * and the quantised KV-cache store that feeds it (msa_kv_store_fp8):
  *   (a) per-tensor e4m3 quantisation of Q and the indexer query
  *       -> msa_quant_fp8
  *   (b) indexer scores reduced per 128-token block, then a strictly
@@ -127,6 +128,48 @@ msa_status msa_check_errors(msa_stream_t stream);
 msa_status msa_quant_fp8(const void* x, msa_dtype x_dtype, int64_t rows, int64_t cols,
                          int64_t x_row_stride, void* out, msa_dtype out_dtype,
                          int64_t out_row_stride, const float* scale, msa_stream_t stream);
+
+/*
+ * The store before the path: quantise the new tokens' K, V and index-K rows
+ * into the paged e4m3 pools. [30971] implementation step 4 (the sparse KV
+ * pool's K / V / index-K stores, each with a per-tensor scale whose absence
+ * means the unit scale and no division) and step 3 (the store runs before
+ * the query quantiser); [45892] implementation step 3 (head-less index-K
+ * cache).
+ *
+ * New token t of sequence b (rows cu_q[b] .. cu_q[b+1]-1, see the batch
+ * description above) sits at position p = seq_lens[b] - q_len_b + (t - cu_q[b]),
+ * physical page pg = page_table[b * max_pages + p / 128], slot s = p % 128:
+ *   k_cache[pg][h][s][:]    = e4m3(fp32(k[t][h][:])  * s_inv_k)
+ *   v_cache[pg][h][s][:]    = e4m3(fp32(v[t][h][:])  * s_inv_v)
+ *   idx_k_cache[pg][s][:]   = e4m3(fp32(idx_k[t][:]) * s_inv_idx)
+ * with the rounding and s_inv rule of msa_quant_fp8. No other byte of the
+ * pools is written. Tokens must address distinct slots.
+ *
+ * k, v:      device, bf16 or fp16 (in_dtype), [T][Hkv][D]; token t at element
+ *            offset t * k_token_stride (v_token_stride), [Hkv][D] contiguous
+ *            within a token (so a slice of a fused QKV row works).
+ * idx_k:     device, [T][d_idx], token stride idx_k_token_stride.
+ *            Any of k, v, idx_k may be NULL: that pool is not touched and its
+ *            cache pointer may be NULL too.
+ * k_cache, v_cache: device, [num_pages][Hkv][128][D] e4m3 (updated in place).
+ * idx_k_cache:      device, [num_pages][128][d_idx] e4m3 (updated in place).
+ * Requirements (MSA_ERR_INVALID_ARG otherwise): D and d_idx positive
+ *   multiples of 16 for the parts given; token strides >= the row and
+ *   multiples of 8 elements; every given input and cache 16-byte aligned;
+ *   B, max_pages, num_pages >= 1. T = 0 returns MSA_OK after these scalar
+ *   checks without reading any pointer.
+ * Data errors (a position with no page-table entry, a page id outside
+ *   [0, num_pages), q_len_b > seq_lens[b], a row beyond cu_q[B]): that token
+ *   is skipped and MSA_ERR_DATA is recorded for msa_check_errors().
+ */
+msa_status msa_kv_store_fp8(const void* k, const void* v, const void* idx_k, msa_dtype in_dtype,
+                            int64_t k_token_stride, int64_t v_token_stride,
+                            int64_t idx_k_token_stride, const int32_t* page_table,
+                            const int32_t* seq_lens, const int32_t* cu_q, int B, int T,
+                            int max_pages, int num_pages, int Hkv, int D, int d_idx,
+                            const float* k_scale, const float* v_scale, const float* idx_k_scale,
+                            void* k_cache, void* v_cache, void* idx_k_cache, msa_stream_t stream);
 
 /* Bytes of device workspace msa_index_topk needs for these sizes. */
 size_t msa_index_topk_workspace_size(int T, int Hidx, int max_pages);

@@ -9,7 +9,8 @@ Sources (the four web pages this method is described on):
 
 * sglang PR 30971 page, "M3 attention GEMMs fully fp8" -- the q/idx_q
   quantiser ``_quant_q_fp8``, the strictly ascending block-id top-k contract
-  and the per-tensor scale semantics (implementation steps 2 and 3).
+  and the per-tensor scale semantics (implementation steps 2 and 3); the
+  paged pool's K / V / index-K stores (step 4).
 * vLLM PR 45892 page, "SM100 MSA indexer backend for MiniMax M3" -- indexer
   scoring reduced per 128-token page (``max_score``), the shared
   ``topk_indices_buffer[index_heads, tokens, topk]`` and the head-less fp8

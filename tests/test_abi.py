@@ -114,3 +114,26 @@ def test_empty_batches_return_ok_without_touching_pointers(lib):
                               null, null, 0, null) == 2                      # d_idx 96
     assert lib.msa_sparse_attn_fwd(null, null, null, null, null, null, null, null, -1.0, None, None, None,
                                    1, 0, 0, 16, 2, 4, 128, 64, 1, 1, null, null, null, null, 0, null) == 1
+
+
+def test_kv_store_validation(lib):
+    p = ctypes.c_void_p(256)
+    null = None
+
+    def call(k=p, v=p, ik=p, dt=0, ks=256, vs=256, iks=128, B=1, T=4, mp=2, npg=8, Hkv=2, D=128, di=128,
+             kscale=None, kc=p, vc=p, ic=p):
+        return lib.msa_kv_store_fp8(k, v, ik, dt, ks, vs, iks, p, p, p, B, T, mp, npg, Hkv, D, di,
+                                    kscale, None, None, kc, vc, ic, None)
+    assert call(dt=2) == 1                        # e4m3 input
+    assert call(D=120) == 1                       # D not a multiple of 16
+    assert call(di=8) == 1                        # d_idx not a multiple of 16
+    assert call(ks=255) == 1                      # token stride below the row
+    assert call(ks=260) == 1                      # token stride not a multiple of 8
+    assert call(kc=null) == 1                     # k given without its cache
+    assert call(k=ctypes.c_void_p(258)) == 1      # misaligned input
+    assert call(kscale=_f(0.0)) == 1              # zero scale
+    assert call(B=0) == 1
+    # T = 0, or no part given: OK without reading a pointer
+    assert lib.msa_kv_store_fp8(null, null, null, 0, 0, 0, 0, null, null, null, 1, 0, 1, 1, 2, 128, 128,
+                                None, None, None, null, null, null, null) == 0
+    assert call(k=null, v=null, ik=null) == 0
