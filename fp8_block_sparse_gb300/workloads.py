@@ -279,3 +279,12 @@ def random_topk(seed: int, seq_lens: np.ndarray, cu_q: np.ndarray, Hidx: int, to
                     out[i, t, :topk - 1] = pick
                     out[i, t, topk - 1] = own
     return out
+
+
+def rotary_table(max_pos: int, d_rope: int, base: float = 10000.0) -> np.ndarray:
+    """A standard rotary cos/sin table as a synthetic input: row p holds the
+    d_rope/2 cosines then the d_rope/2 sines of p * base**(-2i/d_rope),
+    evaluated in float64 and rounded to float32."""
+    inv = base ** (-np.arange(0, d_rope, 2, dtype=np.float64) / d_rope)
+    ang = np.arange(max_pos, dtype=np.float64)[:, None] * inv[None, :]
+    return np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32)
