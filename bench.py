@@ -316,6 +316,30 @@ def mla_measure(msa, wl, dev, steps, flush, pk):
         torch.cuda.synchronize()
         ms.append(a.elapsed_time(b))
     msa.check_errors()
+    # the fused producer of the same q: rotary embedding of q[..., 512:] and
+    # e4m3 of nope || rope(pe), one launch per step
+    cs = t(wl.rotary_table(w.cfg.S_kv, 64))
+    pos = t((np.arange(T) + w.cfg.S_kv - T).astype(np.int32))
+    rq = lambda: msa.rope_quant_fp8(q[..., :512], q[..., 512:], cs, pos, is_neox=True,
+                                    scale=w.scales["q"], out=q8)
+    for _ in range(3):
+        rq()
+    torch.cuda.synchronize()
+    r_ms = []
+    for _ in range(steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        rq()
+        b.record()
+        torch.cuda.synchronize()
+        r_ms.append(a.elapsed_time(b))
+    msa.check_errors()
+    r_bytes = 3 * q.numel() + 4 * T * (64 + 1)
+    rm = statistics.mean(r_ms)
+    rope = {"kernel": "rope_quant_kernel", "rows": T, "heads": H, "d_nope": 512, "d_rope": 64, "ms": rm,
+            "gbs": r_bytes / (rm / 1e3) / 1e9, "frac_of_hbm": r_bytes / (rm / 1e3) / 1e9 / pk["hbm_gbs"],
+            "algorithmic_bytes": r_bytes}
     flops = float(np.sum(w.topk_length.astype(np.float64))) * H * (2 * 576 + 2 * 512)
     k = statistics.mean(kern)
     fp8_peak = 2.0 * pk["bf16_tflops"]
@@ -323,7 +347,7 @@ def mla_measure(msa, wl, dev, steps, flush, pk):
             "tokens_per_s": T / (statistics.mean(ms) / 1e3),
             "kernel": "mla_prefill_kernel", "kernel_ms": k, "tflops_algorithmic": flops / (k / 1e3) / 1e12,
             "frac_of_fp8_peak": flops / (k / 1e3) / 1e12 / fp8_peak, "algorithmic_flop": flops,
-            "peak_basis": f"{pk['source']} bf16 burst x2"}
+            "peak_basis": f"{pk['source']} bf16 burst x2", "rope_quant": rope}
 
 
 def kv_store_measure(msa, w, dev, steps, flush, pk):

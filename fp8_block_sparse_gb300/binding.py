@@ -48,6 +48,8 @@ _SIGNATURES = {
     "msa_quant_fp8": ([_P, _I, _I64, _I64, _I64, _P, _I, _I64, _FP, _P], _I),
     "msa_kv_store_fp8": ([_P, _P, _P, _I, _I64, _I64, _I64, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
                           _FP, _FP, _FP, _P, _P, _P, _P], _I),
+    "msa_rope_quant_fp8": ([_P, _P, _I, _I64, _I, _I, _I, _I64, _I64, _I64, _I64, _P, _I, _P, _I,
+                            _FP, _P, _P], _I),
     "msa_index_topk_workspace_size": ([_I, _I, _I], _SZ),
     "msa_index_topk": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P, _SZ, _P], _I),
     "msa_index_topk_noalloc": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P], _I),
@@ -197,6 +199,44 @@ def kv_store_fp8(page_table: torch.Tensor, seq_lens: torch.Tensor, cu_q: torch.T
                                 _ptr(cu_q), B, T, max_pages, cache.shape[0], Hkv, D, d_idx,
                                 _scale(k_scale), _scale(v_scale), _scale(idx_k_scale),
                                 _ptr(k_cache), _ptr(v_cache), _ptr(idx_k_cache), _stream(stream)))
+
+
+def rope_quant_fp8(nope: Optional[torch.Tensor], pe: torch.Tensor, cos_sin_cache: torch.Tensor,
+                   positions: torch.Tensor, is_neox: bool = True, scale: Optional[float] = None,
+                   out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """e4m3 codes [rows, heads, d_nope + d_rope] of nope || rope(pe).
+
+    nope: [rows, heads, d_nope] (or None when d_nope = 0); pe: [rows, heads or
+    1, d_rope], a single head broadcast to all; last dims contiguous."""
+    lib = load()
+    rows, hp, d_rope = pe.shape
+    heads, d_nope = (nope.shape[1], nope.shape[2]) if nope is not None else (hp, 0)
+    dt = pe.dtype
+    for x, n in ((nope, "nope"), (pe, "pe")):
+        if x is None:
+            continue
+        if not x.is_cuda or x.dtype != dt or dt not in (torch.bfloat16, torch.float16):
+            raise MsaError(1, f"{n} must be a bf16 or fp16 CUDA tensor like pe")
+        if x.dim() != 3 or x.shape[0] != rows or (x.shape[2] > 1 and x.stride(2) != 1):
+            raise MsaError(1, f"{n} must be [rows, heads, d] with a contiguous last dim")
+    if hp not in (1, heads):
+        raise MsaError(1, "pe must have 1 head or as many as nope")
+    _dev(cos_sin_cache, "cos_sin_cache", torch.float32)
+    _dev(positions, "positions", torch.int32)
+    if cos_sin_cache.dim() != 2 or cos_sin_cache.shape[1] != d_rope or positions.numel() != rows:
+        raise MsaError(1, "cos_sin_cache must be [max_pos, d_rope] and positions [rows]")
+    if out is None:
+        out = torch.empty((rows, heads, d_nope + d_rope), dtype=torch.uint8, device=pe.device)
+    _dev(out, "out", torch.uint8)
+    if tuple(out.shape) != (rows, heads, d_nope + d_rope):
+        raise MsaError(1, f"out must be [{rows}, {heads}, {d_nope + d_rope}]")
+    ns = (nope.stride(0), nope.stride(1)) if nope is not None else (0, 0)
+    ps = (pe.stride(0), pe.stride(1) if hp == heads and heads > 1 else 0)
+    _check(lib.msa_rope_quant_fp8(_ptr(nope), _ptr(pe), MSA_BF16 if dt == torch.bfloat16 else MSA_FP16,
+                                  rows, heads, d_nope, d_rope, ns[0], ns[1], ps[0], ps[1],
+                                  _ptr(cos_sin_cache), cos_sin_cache.shape[0], _ptr(positions),
+                                  1 if is_neox else 0, _scale(scale), _ptr(out), _stream(stream)))
+    return out
 
 
 def index_topk_workspace_size(T: int, Hidx: int, max_pages: int) -> int:

@@ -278,6 +278,57 @@ msa_status msa_kv_store_fp8(const void* k, const void* v, const void* idx_k, msa
   return MSA_OK;
 }
 
+msa_status msa_rope_quant_fp8(const void* nope, const void* pe, msa_dtype in_dtype, int64_t rows,
+                              int heads, int d_nope, int d_rope, int64_t nope_token_stride,
+                              int64_t nope_head_stride, int64_t pe_token_stride,
+                              int64_t pe_head_stride, const float* cos_sin_cache, int max_pos,
+                              const int32_t* positions, int is_neox, const float* scale, void* out,
+                              msa_stream_t stream) {
+  const std::string fn = "msa_rope_quant_fp8";
+  if (in_dtype != MSA_BF16 && in_dtype != MSA_FP16)
+    return fail(MSA_ERR_INVALID_ARG, fn + ": in_dtype must be MSA_BF16 or MSA_FP16");
+  if (rows < 0 || heads < 1 || max_pos < 1)
+    return fail(MSA_ERR_INVALID_ARG, fn + ": need rows >= 0, heads >= 1, max_pos >= 1");
+  if (d_nope < 0 || d_nope % 16 != 0 || d_rope < 32 || d_rope % 32 != 0 || d_nope + d_rope > (1 << 16))
+    return fail(MSA_ERR_INVALID_ARG, fn + ": d_nope must be a multiple of 16 and d_rope a positive multiple of 32");
+  float sc = 1.0f;
+  if (!read_scale(scale, &sc, "msa_rope_quant_fp8: scale")) return MSA_ERR_INVALID_ARG;
+  if (rows == 0) return MSA_OK;
+  if (pe == nullptr || cos_sin_cache == nullptr || positions == nullptr || out == nullptr ||
+      (d_nope > 0 && nope == nullptr))
+    return fail(MSA_ERR_INVALID_ARG, fn + ": null pointer");
+  const bool strides_ok = nope_token_stride >= 0 && nope_head_stride >= 0 && pe_token_stride >= 0 &&
+                          pe_head_stride >= 0 && nope_token_stride % 8 == 0 &&
+                          nope_head_stride % 8 == 0 && pe_token_stride % 8 == 0 &&
+                          pe_head_stride % 8 == 0;
+  if (!strides_ok) return fail(MSA_ERR_INVALID_ARG, fn + ": strides must be non-negative multiples of 8 elements");
+  if ((d_nope > 0 && !aligned(nope, 16)) || !aligned(pe, 16) || !aligned(cos_sin_cache, 16) ||
+      !aligned(out, 16))
+    return fail(MSA_ERR_INVALID_ARG, fn + ": nope, pe, cos_sin_cache and out must be 16-byte aligned");
+  RopeQuantArgs a;
+  a.nope = static_cast<const uint16_t*>(nope);
+  a.pe = static_cast<const uint16_t*>(pe);
+  a.nope_tok_stride = nope_token_stride;
+  a.nope_head_stride = nope_head_stride;
+  a.pe_tok_stride = pe_token_stride;
+  a.pe_head_stride = pe_head_stride;
+  a.cos_sin = cos_sin_cache;
+  a.max_pos = max_pos;
+  a.positions = positions;
+  a.rows = rows;
+  a.heads = heads;
+  a.d_nope = d_nope;
+  a.d_rope = d_rope;
+  a.s_inv = scale ? 1.0f / sc : 1.0f;
+  a.out = static_cast<uint8_t*>(out);
+  a.err = device_error_word();
+  if (a.err == nullptr) return fail(MSA_ERR_CUDA, fn + ": no device error word");
+  cudaError_t e = launch_rope_quant(a, in_dtype == MSA_BF16, is_neox != 0,
+                                    reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, fn.c_str());
+  return MSA_OK;
+}
+
 size_t msa_index_topk_workspace_size(int T, int Hidx, int max_pages) {
   if (T < 0 || Hidx < 0 || max_pages < 0) return 0;
   return index_workspace_bytes(T, Hidx, max_pages);

@@ -55,6 +55,23 @@ struct KvStoreArgs {
 };
 cudaError_t launch_kv_store(const KvStoreArgs& a, bool bf16, cudaStream_t stream);
 
+// Fused rotary embedding + quantisation: out[r][h] = e4m3(nope || rope(pe)).
+// Strides in elements; pe_head_stride 0 broadcasts one pe row to every head.
+struct RopeQuantArgs {
+  const uint16_t* nope;
+  const uint16_t* pe;
+  int64_t nope_tok_stride, nope_head_stride, pe_tok_stride, pe_head_stride;
+  const float* cos_sin;      // [max_pos][d_rope]: d_rope/2 cosines, then d_rope/2 sines
+  int max_pos;
+  const int32_t* positions;  // [rows]
+  int64_t rows;
+  int heads, d_nope, d_rope;
+  float s_inv;
+  uint8_t* out;              // [rows][heads][d_nope + d_rope]
+  unsigned* err;
+};
+cudaError_t launch_rope_quant(const RopeQuantArgs& a, bool bf16, bool neox, cudaStream_t stream);
+
 // Step (b). Scores go to `scores` [Hidx][T][max_pages] fp32 (workspace).
 struct IndexArgs {
   const uint8_t* idx_q;

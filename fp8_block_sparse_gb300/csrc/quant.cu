@@ -1,10 +1,14 @@
 // quant.cu -- step (a): per-tensor e4m3 quantisation, out = e4m3(fp32(x) * s_inv),
-// and the quantised KV-cache store that feeds the path with the same rule.
+// the quantised KV-cache store that feeds the path with the same rule, and the
+// fused rotary embedding + quantisation of MLA q / kv rows (nope || rope(pe)).
 //
 // sglang PR 25460 page, key source excerpt of fp8_quantize (widen to fp32,
 // multiply by a host-side scale_inv, cast to fp8); sglang PR 30971 page,
 // implementation step 3 (_quant_q_fp8 on q and idx_q) and step 4 (the sparse KV
-// pool's K / V / index-K stores with per-tensor scales, None = unit scale).
+// pool's K / V / index-K stores with per-tensor scales, None = unit scale);
+// sglang PR 25460 page, implementation step 2 and the _fused_rope_fp8_quantize
+// excerpt (rotary embedding of the pe part, nope and pe written side by side
+// as one e4m3 row).
 //
 // Pure streaming work (2 bytes in, 1 byte out per element), so the kernel is
 // built for HBM: each thread moves 16 elements per step as two 16-byte loads
@@ -222,7 +226,124 @@ __global__ void __launch_bounds__(256) kv_store_kernel(KvStoreArgs a, int tpb) {
   }
 }
 
+// 16 fp32 values * s_inv -> 16 e4m3 codes.
+MSA_DEV uint4 quant16f(const float (&v)[16], float s_inv) {
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    o[i] = uint32_t(cvt2(__fmul_rn(v[4 * i], s_inv), __fmul_rn(v[4 * i + 1], s_inv))) |
+           (uint32_t(cvt2(__fmul_rn(v[4 * i + 2], s_inv), __fmul_rn(v[4 * i + 3], s_inv))) << 16);
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+MSA_DEV void load16f(const float* p, float (&v)[16]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 f = __ldg(reinterpret_cast<const float4*>(p) + i);
+    v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
+  }
+}
+
+// Output chunk j of one (row, head): 16 e4m3 codes of nope || rope(pe). The
+// rotation is fp32 with every product and sum rounded on its own
+// (__fmul_rn / __fadd_rn / __fsub_rn are never contracted into an FMA).
+template <bool BF16, bool NEOX>
+MSA_DEV uint4 rope_chunk(const RopeQuantArgs& a, int64_t r, int h, int j) {
+  const int nn = a.d_nope / 16;
+  if (j < nn) {
+    const uint4* src = reinterpret_cast<const uint4*>(a.nope + r * a.nope_tok_stride +
+                                                      h * a.nope_head_stride + j * 16);
+    return quant16<BF16>(__ldcs(src), __ldcs(src + 1), a.s_inv);
+  }
+  const int e0 = (j - nn) * 16;      // first pe element of this chunk
+  const int pos = __ldg(a.positions + r);
+  if (pos < 0 || pos >= a.max_pos) {
+    atomicOr(a.err, MSA_DEVERR_DATA);
+    return make_uint4(0u, 0u, 0u, 0u);
+  }
+  const int half = a.d_rope / 2;
+  const uint16_t* pe = a.pe + r * a.pe_tok_stride + h * a.pe_head_stride;
+  const float* cs = a.cos_sin + int64_t(pos) * a.d_rope;
+  float x[16], y[16], v[16];
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(pe + e0);
+    widen8<BF16>(__ldg(src), *reinterpret_cast<float(*)[8]>(x));
+    widen8<BF16>(__ldg(src + 1), *reinterpret_cast<float(*)[8]>(x + 8));
+  }
+  if (NEOX) {
+    // halves (x1, x2): out1 = x1 c - x2 s, out2 = x2 c + x1 s, angle = index in the half
+    const bool first = e0 < half;
+    const int i0 = first ? e0 : e0 - half;
+    const uint4* partner = reinterpret_cast<const uint4*>(pe + (first ? e0 + half : e0 - half));
+    widen8<BF16>(__ldg(partner), *reinterpret_cast<float(*)[8]>(y));
+    widen8<BF16>(__ldg(partner + 1), *reinterpret_cast<float(*)[8]>(y + 8));
+    float c[16], sn[16];
+    load16f(cs + i0, c);
+    load16f(cs + half + i0, sn);
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      v[i] = first ? __fsub_rn(__fmul_rn(x[i], c[i]), __fmul_rn(y[i], sn[i]))
+                   : __fadd_rn(__fmul_rn(x[i], c[i]), __fmul_rn(y[i], sn[i]));
+  } else {
+    // neighbour pairs (x[2k], x[2k+1]) at angle e0/2 + k
+    float c[8], sn[8];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const float4 fc = __ldg(reinterpret_cast<const float4*>(cs + e0 / 2) + i);
+      const float4 fs = __ldg(reinterpret_cast<const float4*>(cs + half + e0 / 2) + i);
+      c[4 * i] = fc.x; c[4 * i + 1] = fc.y; c[4 * i + 2] = fc.z; c[4 * i + 3] = fc.w;
+      sn[4 * i] = fs.x; sn[4 * i + 1] = fs.y; sn[4 * i + 2] = fs.z; sn[4 * i + 3] = fs.w;
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      v[2 * k] = __fsub_rn(__fmul_rn(x[2 * k], c[k]), __fmul_rn(x[2 * k + 1], sn[k]));
+      v[2 * k + 1] = __fadd_rn(__fmul_rn(x[2 * k + 1], c[k]), __fmul_rn(x[2 * k], sn[k]));
+    }
+  }
+  return quant16f(v, a.s_inv);
+}
+
+// One thread step = one 16-byte output chunk; two steps in flight.
+template <bool BF16, bool NEOX>
+__global__ void __launch_bounds__(256) rope_quant_kernel(RopeQuantArgs a) {
+  const uint32_t cpr = uint32_t(a.d_nope + a.d_rope) / 16;
+  const uint64_t total = uint64_t(a.rows) * uint64_t(a.heads) * cpr;
+  const uint64_t step = uint64_t(gridDim.x) * blockDim.x;
+  uint4* out = reinterpret_cast<uint4*>(a.out);
+  for (uint64_t c = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x; c < total; c += 2 * step) {
+    const uint64_t c1 = c + step;
+    const uint64_t rh0 = c / cpr;
+    const int j0 = int(c - rh0 * cpr);
+    const int64_t r0 = int64_t(rh0 / uint32_t(a.heads));
+    const uint4 o0 = rope_chunk<BF16, NEOX>(a, r0, int(rh0 - uint64_t(r0) * a.heads), j0);
+    if (c1 < total) {
+      const uint64_t rh1 = c1 / cpr;
+      const int j1 = int(c1 - rh1 * cpr);
+      const int64_t r1 = int64_t(rh1 / uint32_t(a.heads));
+      out[c1] = rope_chunk<BF16, NEOX>(a, r1, int(rh1 - uint64_t(r1) * a.heads), j1);
+    }
+    out[c] = o0;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_rope_quant(const RopeQuantArgs& a, bool bf16, bool neox, cudaStream_t stream) {
+  if (a.rows == 0) return cudaSuccess;
+  const uint64_t total = uint64_t(a.rows) * uint64_t(a.heads) * uint64_t((a.d_nope + a.d_rope) / 16);
+  const int threads = 256;
+  const uint64_t want = (total + 2 * threads - 1) / (2 * threads);
+  const uint64_t cap = uint64_t(num_sms()) * 8;
+  const int grid = int(want < cap ? want : cap);
+  if (bf16) {
+    if (neox) rope_quant_kernel<true, true><<<grid, threads, 0, stream>>>(a);
+    else rope_quant_kernel<true, false><<<grid, threads, 0, stream>>>(a);
+  } else {
+    if (neox) rope_quant_kernel<false, true><<<grid, threads, 0, stream>>>(a);
+    else rope_quant_kernel<false, false><<<grid, threads, 0, stream>>>(a);
+  }
+  return cudaGetLastError();
+}
 
 cudaError_t launch_kv_store(const KvStoreArgs& a, bool bf16, cudaStream_t stream) {
   if (a.T == 0) return cudaSuccess;

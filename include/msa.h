@@ -3,7 +3,8 @@
  * GB300 (sm_103a).
  *
  * The library computes the three steps of the sparse-attention hot path,
- * and the quantised KV-cache store that feeds it (msa_kv_store_fp8):
+ * the quantised KV-cache store that feeds it (msa_kv_store_fp8) and a fused
+ * rotary + quantisation producer of the MLA inputs (msa_rope_quant_fp8):
  *   (a) per-tensor e4m3 quantisation of Q and the indexer query
  *       -> msa_quant_fp8
  *   (b) indexer scores reduced per 128-token block, then a strictly
@@ -170,6 +171,46 @@ msa_status msa_kv_store_fp8(const void* k, const void* v, const void* idx_k, msa
                             int max_pages, int num_pages, int Hkv, int D, int d_idx,
                             const float* k_scale, const float* v_scale, const float* idx_k_scale,
                             void* k_cache, void* v_cache, void* idx_k_cache, msa_stream_t stream);
+
+/*
+ * Fused producer of the sparse-MLA inputs: rotary embedding of the pe part
+ * and e4m3 quantisation of nope || rope(pe) as one row. [25460]
+ * implementation step 2 and the _fused_rope_fp8_quantize excerpt (nope and
+ * rotated pe written side by side, a k_pe shared by all heads broadcast,
+ * neox flag, per-tensor quantisation scale); key source excerpt of
+ * fp8_quantize (widen to fp32, scale, cast).
+ *
+ * For row r (a token), head h, with p = positions[r], C = cos_sin_cache[p][0 .. d_rope/2),
+ * S = cos_sin_cache[p][d_rope/2 .. d_rope):
+ *   is_neox != 0: x1 = pe[.. d_rope/2), x2 = pe[d_rope/2 ..);
+ *                 rot = (x1*C - x2*S, x2*C + x1*S)
+ *   is_neox == 0: pairs (pe[2i], pe[2i+1]) -> (pe[2i]*C[i] - pe[2i+1]*S[i],
+ *                 pe[2i+1]*C[i] + pe[2i]*S[i])
+ *   out[r][h][0 .. d_nope)               = e4m3(fp32(nope[r][h][:]) * s_inv)
+ *   out[r][h][d_nope .. d_nope + d_rope) = e4m3(rot * s_inv)
+ * in fp32 with every product and sum rounded on its own (no FMA), s_inv as in
+ * msa_quant_fp8 (NULL scale = no multiply), the same RNE-satfinite cast.
+ *
+ * nope:  device, bf16/fp16 [rows][heads][d_nope]; element (r, h, i) at
+ *        r * nope_token_stride + h * nope_head_stride + i. May be NULL when
+ *        d_nope = 0.
+ * pe:    device, same dtype, [rows][heads][d_rope] with its own strides;
+ *        pe_head_stride = 0 broadcasts one pe row (a shared k_pe) to all heads.
+ * cos_sin_cache: device fp32 [max_pos][d_rope]; positions: device int32 [rows].
+ * out:   device, e4m3 [rows][heads][d_nope + d_rope], contiguous, written in full.
+ * Requirements (MSA_ERR_INVALID_ARG otherwise): d_nope a multiple of 16,
+ *   d_rope a positive multiple of 32, strides non-negative multiples of 8,
+ *   nope / pe / cos_sin_cache / out 16-byte aligned. rows = 0 returns MSA_OK
+ *   after the scalar checks without reading any pointer.
+ * A position outside [0, max_pos) writes zeros to that row's rope part and
+ *   records MSA_ERR_DATA for msa_check_errors().
+ */
+msa_status msa_rope_quant_fp8(const void* nope, const void* pe, msa_dtype in_dtype, int64_t rows,
+                              int heads, int d_nope, int d_rope, int64_t nope_token_stride,
+                              int64_t nope_head_stride, int64_t pe_token_stride,
+                              int64_t pe_head_stride, const float* cos_sin_cache, int max_pos,
+                              const int32_t* positions, int is_neox, const float* scale, void* out,
+                              msa_stream_t stream);
 
 /* Bytes of device workspace msa_index_topk needs for these sizes. */
 size_t msa_index_topk_workspace_size(int T, int Hidx, int max_pages);

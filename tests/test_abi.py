@@ -137,3 +137,25 @@ def test_kv_store_validation(lib):
     assert lib.msa_kv_store_fp8(null, null, null, 0, 0, 0, 0, null, null, null, 1, 0, 1, 1, 2, 128, 128,
                                 None, None, None, null, null, null, null) == 0
     assert call(k=null, v=null, ik=null) == 0
+
+
+def test_rope_quant_validation(lib):
+    p = ctypes.c_void_p(256)
+    null = None
+
+    def call(nope=p, pe=p, dt=0, rows=4, heads=2, dn=128, dr=64, ns=256, pe_s=128, ph=64, cs=p, mp=10,
+             scale=None, out=p):
+        return lib.msa_rope_quant_fp8(nope, pe, dt, rows, heads, dn, dr, ns, dn, pe_s, ph, cs, mp, p, 1,
+                                      scale, out, None)
+    assert call(dt=2) == 1                        # e4m3 input
+    assert call(dn=120) == 1                      # d_nope not a multiple of 16
+    assert call(dr=48) == 1                       # d_rope not a multiple of 32
+    assert call(ns=260) == 1                      # stride not a multiple of 8
+    assert call(ph=-8) == 1
+    assert call(out=ctypes.c_void_p(264)) == 1    # misaligned output
+    assert call(mp=0) == 1
+    assert call(scale=_f(float("inf"))) == 1
+    assert call(heads=0) == 1
+    # rows = 0: OK without reading any pointer
+    assert lib.msa_rope_quant_fp8(null, null, 0, 0, 2, 128, 64, 0, 0, 0, 0, null, 1, null, 1,
+                                  None, null, null) == 0
