@@ -244,42 +244,76 @@ MSA_DEV void load16f(const float* p, float (&v)[16]) {
   }
 }
 
-// Output chunk j of one (row, head): 16 e4m3 codes of nope || rope(pe). The
-// rotation is fp32 with every product and sum rounded on its own
-// (__fmul_rn / __fadd_rn / __fsub_rn are never contracted into an FMA).
+// One output chunk (16 e4m3 codes of nope || rope(pe)) in two phases: fetch
+// issues every global load of the chunk, finish does the arithmetic, so a
+// thread keeps several chunks' loads in flight before it waits on any.
+struct RopeChunk {
+  uint4 lo, hi;     // the chunk's own 16 inputs
+  uint4 plo, phi;   // neox: the partner half's 16 inputs
+  const float* cs;  // table row of the position (rope chunks)
+  uint4* dst;       // null: nothing to write
+  int e0;           // first pe element (-1: nope chunk)
+  bool bad;         // position outside the table
+};
+
 template <bool BF16, bool NEOX>
-MSA_DEV uint4 rope_chunk(const RopeQuantArgs& a, int64_t r, int h, int j) {
+MSA_DEV void rope_fetch(const RopeQuantArgs& a, int64_t r, int h, int j, uint4* dst, RopeChunk& k) {
   const int nn = a.d_nope / 16;
+  k.dst = dst;
+  k.bad = false;
   if (j < nn) {
     const uint4* src = reinterpret_cast<const uint4*>(a.nope + r * a.nope_tok_stride +
                                                       h * a.nope_head_stride + j * 16);
-    return quant16<BF16>(__ldcs(src), __ldcs(src + 1), a.s_inv);
+    k.e0 = -1;
+    k.lo = __ldcs(src);
+    k.hi = __ldcs(src + 1);
+    return;
   }
-  const int e0 = (j - nn) * 16;      // first pe element of this chunk
+  k.e0 = (j - nn) * 16;
   const int pos = __ldg(a.positions + r);
   if (pos < 0 || pos >= a.max_pos) {
-    atomicOr(a.err, MSA_DEVERR_DATA);
-    return make_uint4(0u, 0u, 0u, 0u);
+    k.bad = true;
+    return;
   }
   const int half = a.d_rope / 2;
   const uint16_t* pe = a.pe + r * a.pe_tok_stride + h * a.pe_head_stride;
-  const float* cs = a.cos_sin + int64_t(pos) * a.d_rope;
-  float x[16], y[16], v[16];
-  {
-    const uint4* src = reinterpret_cast<const uint4*>(pe + e0);
-    widen8<BF16>(__ldg(src), *reinterpret_cast<float(*)[8]>(x));
-    widen8<BF16>(__ldg(src + 1), *reinterpret_cast<float(*)[8]>(x + 8));
+  k.cs = a.cos_sin + int64_t(pos) * a.d_rope;
+  const uint4* src = reinterpret_cast<const uint4*>(pe + k.e0);
+  k.lo = __ldg(src);
+  k.hi = __ldg(src + 1);
+  if (NEOX) {
+    const uint4* partner = reinterpret_cast<const uint4*>(pe + (k.e0 < half ? k.e0 + half : k.e0 - half));
+    k.plo = __ldg(partner);
+    k.phi = __ldg(partner + 1);
   }
+}
+
+// The rotation is fp32 with every product and sum rounded on its own
+// (__fmul_rn / __fadd_rn / __fsub_rn are never contracted into an FMA).
+template <bool BF16, bool NEOX>
+MSA_DEV void rope_finish(const RopeQuantArgs& a, const RopeChunk& k) {
+  if (k.e0 < 0) {
+    *k.dst = quant16<BF16>(k.lo, k.hi, a.s_inv);
+    return;
+  }
+  if (k.bad) {
+    atomicOr(a.err, MSA_DEVERR_DATA);
+    *k.dst = make_uint4(0u, 0u, 0u, 0u);
+    return;
+  }
+  const int half = a.d_rope / 2;
+  float x[16], v[16];
+  widen8<BF16>(k.lo, *reinterpret_cast<float(*)[8]>(x));
+  widen8<BF16>(k.hi, *reinterpret_cast<float(*)[8]>(x + 8));
   if (NEOX) {
     // halves (x1, x2): out1 = x1 c - x2 s, out2 = x2 c + x1 s, angle = index in the half
-    const bool first = e0 < half;
-    const int i0 = first ? e0 : e0 - half;
-    const uint4* partner = reinterpret_cast<const uint4*>(pe + (first ? e0 + half : e0 - half));
-    widen8<BF16>(__ldg(partner), *reinterpret_cast<float(*)[8]>(y));
-    widen8<BF16>(__ldg(partner + 1), *reinterpret_cast<float(*)[8]>(y + 8));
-    float c[16], sn[16];
-    load16f(cs + i0, c);
-    load16f(cs + half + i0, sn);
+    const bool first = k.e0 < half;
+    const int i0 = first ? k.e0 : k.e0 - half;
+    float y[16], c[16], sn[16];
+    widen8<BF16>(k.plo, *reinterpret_cast<float(*)[8]>(y));
+    widen8<BF16>(k.phi, *reinterpret_cast<float(*)[8]>(y + 8));
+    load16f(k.cs + i0, c);
+    load16f(k.cs + half + i0, sn);
 #pragma unroll
     for (int i = 0; i < 16; ++i)
       v[i] = first ? __fsub_rn(__fmul_rn(x[i], c[i]), __fmul_rn(y[i], sn[i]))
@@ -289,40 +323,83 @@ MSA_DEV uint4 rope_chunk(const RopeQuantArgs& a, int64_t r, int h, int j) {
     float c[8], sn[8];
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-      const float4 fc = __ldg(reinterpret_cast<const float4*>(cs + e0 / 2) + i);
-      const float4 fs = __ldg(reinterpret_cast<const float4*>(cs + half + e0 / 2) + i);
+      const float4 fc = __ldg(reinterpret_cast<const float4*>(k.cs + k.e0 / 2) + i);
+      const float4 fs = __ldg(reinterpret_cast<const float4*>(k.cs + half + k.e0 / 2) + i);
       c[4 * i] = fc.x; c[4 * i + 1] = fc.y; c[4 * i + 2] = fc.z; c[4 * i + 3] = fc.w;
       sn[4 * i] = fs.x; sn[4 * i + 1] = fs.y; sn[4 * i + 2] = fs.z; sn[4 * i + 3] = fs.w;
     }
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      v[2 * k] = __fsub_rn(__fmul_rn(x[2 * k], c[k]), __fmul_rn(x[2 * k + 1], sn[k]));
-      v[2 * k + 1] = __fadd_rn(__fmul_rn(x[2 * k + 1], c[k]), __fmul_rn(x[2 * k], sn[k]));
+    for (int q = 0; q < 8; ++q) {
+      v[2 * q] = __fsub_rn(__fmul_rn(x[2 * q], c[q]), __fmul_rn(x[2 * q + 1], sn[q]));
+      v[2 * q + 1] = __fadd_rn(__fmul_rn(x[2 * q + 1], c[q]), __fmul_rn(x[2 * q], sn[q]));
     }
   }
-  return quant16f(v, a.s_inv);
+  *k.dst = quant16f(v, a.s_inv);
 }
 
-// One thread step = one 16-byte output chunk; two steps in flight.
+// Two block roles in one launch. Blocks [0, nb_nope) quantise the nope
+// chunks: each owns `upb_n` consecutive (row, head) units and streams their
+// d_nope/16 chunks with four in flight per thread (a strided copy with a
+// cast). The remaining blocks own `upb_r` units each and rotate + quantise
+// their d_rope/16 pe chunks, two in flight. Chunk indices inside a block are
+// 32-bit; a unit's (row, head) follows from the block's first unit by small
+// 32-bit steps.
 template <bool BF16, bool NEOX>
-__global__ void __launch_bounds__(256) rope_quant_kernel(RopeQuantArgs a) {
-  const uint32_t cpr = uint32_t(a.d_nope + a.d_rope) / 16;
-  const uint64_t total = uint64_t(a.rows) * uint64_t(a.heads) * cpr;
-  const uint64_t step = uint64_t(gridDim.x) * blockDim.x;
-  uint4* out = reinterpret_cast<uint4*>(a.out);
-  for (uint64_t c = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x; c < total; c += 2 * step) {
-    const uint64_t c1 = c + step;
-    const uint64_t rh0 = c / cpr;
-    const int j0 = int(c - rh0 * cpr);
-    const int64_t r0 = int64_t(rh0 / uint32_t(a.heads));
-    const uint4 o0 = rope_chunk<BF16, NEOX>(a, r0, int(rh0 - uint64_t(r0) * a.heads), j0);
-    if (c1 < total) {
-      const uint64_t rh1 = c1 / cpr;
-      const int j1 = int(c1 - rh1 * cpr);
-      const int64_t r1 = int64_t(rh1 / uint32_t(a.heads));
-      out[c1] = rope_chunk<BF16, NEOX>(a, r1, int(rh1 - uint64_t(r1) * a.heads), j1);
+__global__ void __launch_bounds__(256) rope_quant_kernel(RopeQuantArgs a, int upb_n, int nb_nope,
+                                                         int upb_r) {
+  const int nn = a.d_nope / 16, nr = a.d_rope / 16, cpr = nn + nr;
+  const int64_t units = a.rows * int64_t(a.heads);
+  const bool nope_role = int(blockIdx.x) < nb_nope;
+  const int upb = nope_role ? upb_n : upb_r;
+  const int per = nope_role ? nn : nr;
+  const int64_t u0 = int64_t(nope_role ? blockIdx.x : blockIdx.x - nb_nope) * upb;
+  const int nu = int(units - u0 < upb ? units - u0 : upb);
+  const int64_t r0 = u0 / a.heads;
+  const int h0 = int(u0 - r0 * a.heads);
+  const int total = nu * per;
+  uint4* out = reinterpret_cast<uint4*>(a.out) + u0 * cpr;
+  if (nope_role) {
+    constexpr int U = 4;
+    for (int c0 = threadIdx.x; c0 < total; c0 += U * 256) {
+      uint4 lo[U], hi[U];
+      uint4* dst[U];
+#pragma unroll
+      for (int i = 0; i < U; ++i) {
+        const int c = c0 + i * 256;
+        dst[i] = nullptr;
+        if (c < total) {
+          const int u = c / nn, j = c - u * nn;
+          const int hh = h0 + u, dr = hh / a.heads;
+          const uint4* src = reinterpret_cast<const uint4*>(
+              a.nope + (r0 + dr) * a.nope_tok_stride + (hh - dr * a.heads) * a.nope_head_stride + j * 16);
+          lo[i] = __ldcs(src);
+          hi[i] = __ldcs(src + 1);
+          dst[i] = out + int64_t(u) * cpr + j;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < U; ++i)
+        if (dst[i]) *dst[i] = quant16<BF16>(lo[i], hi[i], a.s_inv);
     }
-    out[c] = o0;
+  } else {
+    constexpr int U = 2;
+    for (int c0 = threadIdx.x; c0 < total; c0 += U * 256) {
+      RopeChunk k[U];
+#pragma unroll
+      for (int i = 0; i < U; ++i) {
+        const int c = c0 + i * 256;
+        k[i].dst = nullptr;
+        if (c < total) {
+          const int u = c / nr, j = c - u * nr;
+          const int hh = h0 + u, dr = hh / a.heads;
+          rope_fetch<BF16, NEOX>(a, r0 + dr, hh - dr * a.heads, nn + j, out + int64_t(u) * cpr + nn + j,
+                                 k[i]);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < U; ++i)
+        if (k[i].dst) rope_finish<BF16, NEOX>(a, k[i]);
+    }
   }
 }
 
@@ -330,17 +407,22 @@ __global__ void __launch_bounds__(256) rope_quant_kernel(RopeQuantArgs a) {
 
 cudaError_t launch_rope_quant(const RopeQuantArgs& a, bool bf16, bool neox, cudaStream_t stream) {
   if (a.rows == 0) return cudaSuccess;
-  const uint64_t total = uint64_t(a.rows) * uint64_t(a.heads) * uint64_t((a.d_nope + a.d_rope) / 16);
-  const int threads = 256;
-  const uint64_t want = (total + 2 * threads - 1) / (2 * threads);
-  const uint64_t cap = uint64_t(num_sms()) * 8;
-  const int grid = int(want < cap ? want : cap);
+  const int nn = a.d_nope / 16, nr = a.d_rope / 16;
+  const int64_t units = a.rows * int64_t(a.heads);
+  // about 2048 chunks (8 per thread) per block of either role
+  const int upb_n = nn > 0 ? (2048 / nn > 0 ? 2048 / nn : 1) : 1;
+  const int upb_r = 2048 / nr > 0 ? 2048 / nr : 1;
+  const int64_t nb_nope = nn > 0 ? (units + upb_n - 1) / upb_n : 0;
+  const int64_t grid = nb_nope + (units + upb_r - 1) / upb_r;
+  if (grid > 0x7fffffffll) return cudaErrorInvalidValue;
+  const unsigned g = unsigned(grid);
+  const int nb = int(nb_nope);
   if (bf16) {
-    if (neox) rope_quant_kernel<true, true><<<grid, threads, 0, stream>>>(a);
-    else rope_quant_kernel<true, false><<<grid, threads, 0, stream>>>(a);
+    if (neox) rope_quant_kernel<true, true><<<g, 256, 0, stream>>>(a, upb_n, nb, upb_r);
+    else rope_quant_kernel<true, false><<<g, 256, 0, stream>>>(a, upb_n, nb, upb_r);
   } else {
-    if (neox) rope_quant_kernel<false, true><<<grid, threads, 0, stream>>>(a);
-    else rope_quant_kernel<false, false><<<grid, threads, 0, stream>>>(a);
+    if (neox) rope_quant_kernel<false, true><<<g, 256, 0, stream>>>(a, upb_n, nb, upb_r);
+    else rope_quant_kernel<false, false><<<g, 256, 0, stream>>>(a, upb_n, nb, upb_r);
   }
   return cudaGetLastError();
 }
