@@ -6,8 +6,11 @@ One step = the whole hot path over one batch of the 32k prefill workload
 64 blocks of 128 tokens): quantise Q and idx_q, index scores + ascending
 top-k, sparse attention with sink. The metric is prefill tokens/s; the same
 line reports the attention kernel's algorithmic TFLOP/s against the FP8
-tensor peak, the paged-decode workload's HBM GB/s, an end-to-end figure with
-host buffers, and the CPU oracle timed on a bounded sample.
+tensor peak, the paged-decode workload's HBM GB/s (eager and as one CUDA
+graph replay), the sparse-MLA kernel with its fused rope + e4m3 producer, the
+quantised KV-cache store of the prefill and decode workloads' new tokens, an
+end-to-end figure with host buffers, and the CPU oracle timed on a bounded
+sample.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
 
