@@ -97,13 +97,33 @@ def _stream(stream: Optional[torch.cuda.Stream]):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def _dev(t: torch.Tensor, name: str, dtype=None) -> None:
-    if not t.is_cuda:
+def _on_device(t: torch.Tensor) -> bool:
+    return t.is_cuda
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None, shape=None) -> None:
+    """A device tensor of this dtype, contiguous, and of this shape (when given):
+    the library reads and writes exactly that extent, so a smaller or host
+    buffer is refused here instead of becoming an out-of-bounds access."""
+    if not _on_device(t):
         raise MsaError(1, f"{name} must be a CUDA tensor")
     if dtype is not None and t.dtype != dtype:
         raise MsaError(1, f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
         raise MsaError(1, f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise MsaError(1, f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _batch(page_table: torch.Tensor, seq_lens: torch.Tensor, cu_q: torch.Tensor):
+    """(B, max_pages) of a batch description, with its three tensors checked."""
+    if page_table.dim() != 2:
+        raise MsaError(1, "page_table must be [B, max_pages]")
+    B, max_pages = page_table.shape
+    _dev(page_table, "page_table", torch.int32)
+    _dev(seq_lens, "seq_lens", torch.int32, (B,))
+    _dev(cu_q, "cu_q", torch.int32, (B + 1,))
+    return B, max_pages
 
 
 def check_errors(stream: Optional[torch.cuda.Stream] = None) -> None:
@@ -129,6 +149,8 @@ def quant_fp8(x: torch.Tensor, scale: Optional[float] = None, out: Optional[torc
     lib = load()
     if x.dtype not in (torch.bfloat16, torch.float16):
         raise MsaError(1, f"x must be bf16 or fp16, got {x.dtype}")
+    if not _on_device(x):
+        raise MsaError(1, "x must be a CUDA tensor")
     if x.stride(-1) != 1:
         raise MsaError(1, "x must have a contiguous last dimension")
     cols = x.shape[-1]
@@ -136,6 +158,9 @@ def quant_fp8(x: torch.Tensor, scale: Optional[float] = None, out: Optional[torc
     x2 = x.reshape(rows, cols) if x.dim() != 2 else x
     if out is None:
         out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    _dev(out, "out", torch.uint8)
+    if out.numel() != x.numel():
+        raise MsaError(1, f"out must hold {x.numel()} elements, got {out.numel()}")
     o2 = out.view(rows, cols)
     _check(lib.msa_quant_fp8(_ptr(x2), MSA_BF16 if x.dtype == torch.bfloat16 else MSA_FP16,
                              rows, cols, x2.stride(0) if rows else cols, _ptr(o2), MSA_E4M3,
@@ -147,7 +172,7 @@ def _token_rows(x: Optional[torch.Tensor], name: str, inner: int):
     """Token stride of x, whose per-token block of `inner` elements is contiguous."""
     if x is None:
         return 0
-    if not x.is_cuda or x.dtype not in (torch.bfloat16, torch.float16):
+    if not _on_device(x) or x.dtype not in (torch.bfloat16, torch.float16):
         raise MsaError(1, f"{name} must be a bf16 or fp16 CUDA tensor")
     want, acc = [], 1
     for n in reversed(x.shape[1:]):
@@ -173,8 +198,7 @@ def kv_store_fp8(page_table: torch.Tensor, seq_lens: torch.Tensor, cu_q: torch.T
     dt = given[0].dtype
     if any(x.dtype != dt for x in given):
         raise MsaError(1, "k, v and idx_k must share one dtype")
-    for t, n in ((page_table, "page_table"), (seq_lens, "seq_lens"), (cu_q, "cu_q")):
-        _dev(t, n, torch.int32)
+    B, max_pages = _batch(page_table, seq_lens, cu_q)
     for c, n in ((k_cache, "k_cache"), (v_cache, "v_cache"), (idx_k_cache, "idx_k_cache")):
         if c is not None:
             _dev(c, n, torch.uint8)
@@ -191,7 +215,6 @@ def kv_store_fp8(page_table: torch.Tensor, seq_lens: torch.Tensor, cu_q: torch.T
     for _, c, n, shape in parts:
         if tuple(c.shape[1:]) != shape or c.shape[0] != cache.shape[0]:
             raise MsaError(1, f"{n} must be [num_pages, {', '.join(map(str, shape))}], got {tuple(c.shape)}")
-    B, max_pages = page_table.shape
     _check(lib.msa_kv_store_fp8(_ptr(k), _ptr(v), _ptr(idx_k),
                                 MSA_BF16 if dt == torch.bfloat16 else MSA_FP16,
                                 _token_rows(k, "k", Hkv * D), _token_rows(v, "v", Hkv * D),
@@ -215,7 +238,7 @@ def rope_quant_fp8(nope: Optional[torch.Tensor], pe: torch.Tensor, cos_sin_cache
     for x, n in ((nope, "nope"), (pe, "pe")):
         if x is None:
             continue
-        if not x.is_cuda or x.dtype != dt or dt not in (torch.bfloat16, torch.float16):
+        if not _on_device(x) or x.dtype != dt or dt not in (torch.bfloat16, torch.float16):
             raise MsaError(1, f"{n} must be a bf16 or fp16 CUDA tensor like pe")
         if x.dim() != 3 or x.shape[0] != rows or (x.shape[2] > 1 and x.stride(2) != 1):
             raise MsaError(1, f"{n} must be [rows, heads, d] with a contiguous last dim")
@@ -251,16 +274,16 @@ def index_topk(idx_q: torch.Tensor, idx_k_cache: torch.Tensor, page_table: torch
     lib = load()
     T, Hidx, D = idx_q.shape
     num_pages = idx_k_cache.shape[0]
-    B, max_pages = page_table.shape
-    for t, n in ((idx_q, "idx_q"), (idx_k_cache, "idx_k_cache")):
-        _dev(t, n, torch.uint8)
-    for t, n in ((page_table, "page_table"), (seq_lens, "seq_lens"), (cu_q, "cu_q")):
-        _dev(t, n, torch.int32)
+    _dev(idx_q, "idx_q", torch.uint8)
+    _dev(idx_k_cache, "idx_k_cache", torch.uint8, (num_pages, 128, D))
+    B, max_pages = _batch(page_table, seq_lens, cu_q)
     if out is None:
         out = torch.empty((Hidx, T, topk), dtype=torch.int32, device=idx_q.device)
+    _dev(out, "out", torch.int32, (Hidx, T, topk))
     ws_bytes = index_topk_workspace_size(T, Hidx, max_pages)
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=idx_q.device)
+    _dev(workspace, "workspace", torch.uint8)
     _check(lib.msa_index_topk(_ptr(idx_q), _ptr(idx_k_cache), _ptr(page_table), _ptr(seq_lens),
                               _ptr(cu_q), B, T, max_q_len, Hidx, D, topk, num_pages, max_pages,
                               _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)))
@@ -275,13 +298,12 @@ def index_topk_noalloc(idx_q: torch.Tensor, idx_k_cache: torch.Tensor, page_tabl
     lib = load()
     T, Hidx, D = idx_q.shape
     num_pages = idx_k_cache.shape[0]
-    B, max_pages = page_table.shape
-    for t, n in ((idx_q, "idx_q"), (idx_k_cache, "idx_k_cache")):
-        _dev(t, n, torch.uint8)
-    for t, n in ((page_table, "page_table"), (seq_lens, "seq_lens"), (cu_q, "cu_q")):
-        _dev(t, n, torch.int32)
+    _dev(idx_q, "idx_q", torch.uint8)
+    _dev(idx_k_cache, "idx_k_cache", torch.uint8, (num_pages, 128, D))
+    B, max_pages = _batch(page_table, seq_lens, cu_q)
     if out is None:
         out = torch.empty((Hidx, T, topk), dtype=torch.int32, device=idx_q.device)
+    _dev(out, "out", torch.int32, (Hidx, T, topk))
     _check(lib.msa_index_topk_noalloc(_ptr(idx_q), _ptr(idx_k_cache), _ptr(page_table), _ptr(seq_lens),
                                       _ptr(cu_q), B, T, max_q_len, Hidx, D, topk, num_pages, max_pages,
                                       _ptr(out), _stream(stream)))
@@ -302,23 +324,28 @@ def sparse_attn_fwd(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tenso
     """Sparse GQA attention (steps a4/a5). Returns (out bf16, max_logit, lse)."""
     lib = load()
     T, Hq, D = q.shape
+    if k_cache.dim() != 4 or topk_indices.dim() != 3:
+        raise MsaError(1, "k_cache must be [num_pages, Hkv, 128, D] and topk_indices [Hidx, T, topk]")
     num_pages, Hkv = k_cache.shape[0], k_cache.shape[1]
     Hidx, _, topk = topk_indices.shape
-    B, max_pages = page_table.shape
-    for t, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
-        _dev(t, n, torch.uint8)
-    for t, n in ((page_table, "page_table"), (seq_lens, "seq_lens"), (cu_q, "cu_q"),
-                 (topk_indices, "topk_indices")):
-        _dev(t, n, torch.int32)
+    _dev(q, "q", torch.uint8)
+    _dev(k_cache, "k_cache", torch.uint8, (num_pages, Hkv, 128, D))
+    _dev(v_cache, "v_cache", torch.uint8, (num_pages, Hkv, 128, D))
+    B, max_pages = _batch(page_table, seq_lens, cu_q)
+    _dev(topk_indices, "topk_indices", torch.int32, (Hidx, T, topk))
     if sink is not None:
-        _dev(sink, "sink", torch.float32)
+        _dev(sink, "sink", torch.float32, (Hq,))
     dev = q.device
     out = torch.empty((T, Hq, D), dtype=torch.bfloat16, device=dev) if out is None else out
     max_logit = torch.empty((T, Hq), dtype=torch.float32, device=dev) if max_logit is None else max_logit
     lse = torch.empty((T, Hq), dtype=torch.float32, device=dev) if lse is None else lse
+    _dev(out, "out", torch.bfloat16, (T, Hq, D))
+    _dev(max_logit, "max_logit", torch.float32, (T, Hq))
+    _dev(lse, "lse", torch.float32, (T, Hq))
     ws_bytes = sparse_attn_workspace_size(B, T, max_q_len, Hq, Hkv, Hidx, topk, max_pages)
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    _dev(workspace, "workspace", torch.uint8)
     _check(lib.msa_sparse_attn_fwd(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table), _ptr(seq_lens), _ptr(cu_q),
         _ptr(topk_indices), _ptr(sink), float(sm_scale), _scale(q_scale), _scale(k_scale),
@@ -336,18 +363,23 @@ def sparse_mla_fwd(q: torch.Tensor, kv: torch.Tensor, indices: torch.Tensor,
     lib = load()
     T, H, d_qk = q.shape
     S_kv = kv.shape[0]
+    if indices.dim() != 2:
+        raise MsaError(1, "indices must be [T, topk]")
     topk = indices.shape[1]
     _dev(q, "q", torch.uint8)
-    _dev(kv, "kv", torch.uint8)
-    _dev(indices, "indices", torch.int32)
+    _dev(kv, "kv", torch.uint8, (S_kv, d_qk))
+    _dev(indices, "indices", torch.int32, (T, topk))
     if topk_length is not None:
-        _dev(topk_length, "topk_length", torch.int32)
+        _dev(topk_length, "topk_length", torch.int32, (T,))
     if sink is not None:
-        _dev(sink, "sink", torch.float32)
+        _dev(sink, "sink", torch.float32, (H,))
     dev = q.device
     out = torch.empty((T, H, d_v), dtype=torch.bfloat16, device=dev) if out is None else out
     max_logits = torch.empty((T, H), dtype=torch.float32, device=dev) if max_logits is None else max_logits
     lse = torch.empty((T, H), dtype=torch.float32, device=dev) if lse is None else lse
+    _dev(out, "out", torch.bfloat16, (T, H, d_v))
+    _dev(max_logits, "max_logits", torch.float32, (T, H))
+    _dev(lse, "lse", torch.float32, (T, H))
     _check(lib.msa_sparse_mla_fwd(_ptr(q), _ptr(kv), _ptr(indices), _ptr(topk_length), _ptr(sink),
                                   float(sm_scale), _scale(q_scale), _scale(kv_scale), T, H, S_kv,
                                   d_qk, d_v, topk, _ptr(out), _ptr(max_logits), _ptr(lse),
