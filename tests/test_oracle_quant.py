@@ -59,3 +59,19 @@ def test_scale_is_applied_as_fp32_inverse_then_one_multiply():
     # and rounds to the even code 0x38 (1.0)
     assert quant.quantize(_bf16([2.125]), 2.0)[0] == 0x38
     assert quant.quantize(_bf16([2.375]), 2.0)[0] == 0x3A   # 1.1875 -> 1.25 (even)
+
+
+def test_scale_inverse_is_the_fp32_reciprocal_of_the_fp32_scale():
+    # reading 1 (sglang PR 25460 page, fp8_quantize excerpt: a host-side
+    # scale_inv): one IEEE single division of 1 by the scale rounded to fp32,
+    # checked against torch's fp32 division
+    g = np.random.default_rng(9)
+    scales = np.concatenate([g.uniform(1e-4, 10.0, 4000), [0.0123, 3.7, 1.0 / 448, 0.1, 1.0 / 3]])
+    want = (torch.ones(len(scales), dtype=torch.float32) /
+            torch.from_numpy(scales).to(torch.float32)).numpy()
+    got = np.array([quant.scale_inverse(float(s)) for s in scales], dtype=np.float32)
+    np.testing.assert_array_equal(got.view(np.uint32), want.view(np.uint32))
+    # the check is sensitive: dividing in float64 first rounds differently for some scales
+    f64_first = np.array([np.float32(1.0 / s) for s in scales], dtype=np.float32)
+    assert np.any(f64_first.view(np.uint32) != want.view(np.uint32))
+    assert quant.scale_inverse(None) == np.float32(1.0)
