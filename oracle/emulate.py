@@ -23,8 +23,10 @@ float64 result can be predicted on the CPU:
 Where the kernels' design fixes it: the prefill kernel keeps P in f16 and
 moves the reference to the block maximum (limit 8, head 0); the decode kernel
 splits P into three e4m3 terms and moves the reference to 4 below the
-maximum (limit 8, head 4). MUFU's approximation error and the MMA's exact
-accumulation order are not modelled (both well below the roundings above).
+maximum (limit 8, head 4); the sparse-MLA kernel walks each query's index
+list in 64-entry chunks with f16 P (limit 8, head 0). MUFU's approximation
+error and the MMA's exact accumulation order are not modelled (both well
+below the roundings above).
 
 The sources of the method are those of ``attention.py``; the pages name fp8
 P as the main error source of an fp8 attention and test it at 6e-2..1e-1
@@ -141,4 +143,35 @@ def emulate_attention(q: np.ndarray, k_pool: np.ndarray, v_pool: np.ndarray,
             sig = None if sink is None else float(np.float32(c * float(sink[h]) * LOG2E))
             out[n, h], max_logit[n, h], lse[n, h] = emulate_row(
                 qd[h], kk, vv, blk, c_qk_log2, sig, vs, p_format, limit, head, round_out)
+    return out, max_logit, lse
+
+
+def emulate_mla(q: np.ndarray, kv: np.ndarray, indices: np.ndarray,
+                topk_length: Optional[np.ndarray], sink: Optional[np.ndarray], sm_scale: float,
+                q_scale: Optional[float] = None, kv_scale: Optional[float] = None, d_v: int = 512,
+                tokens: Optional[Iterable[int]] = None, p_format: str = "f16", limit: float = 8.0,
+                head: float = 0.0, chunk: int = 64, round_out: bool = True):
+    """Emulated sparse MLA with the layouts of ``mla.sparse_mla``: the index
+    list is walked in ``chunk``-entry pieces (the blocks of the lazy softmax)."""
+    T, h, _ = q.shape
+    tok = np.arange(T) if tokens is None else np.asarray(list(tokens), dtype=np.int64)
+    c = float(sm_scale) * unit(q_scale)
+    kvs = unit(kv_scale)
+    c_qk_log2 = float(np.float32(c * kvs * LOG2E))
+    out = np.zeros((len(tok), h, d_v))
+    max_logit = np.zeros((len(tok), h))
+    lse = np.zeros((len(tok), h))
+    for n, t in enumerate(tok):
+        row = indices[t]
+        if topk_length is not None:
+            row = row[: int(topk_length[t])]
+        where = np.nonzero(row >= 0)[0]
+        rows = row[where].astype(np.int64)
+        kk = e4m3.decode(kv[rows])
+        vv = e4m3.decode(kv[rows, :d_v])
+        qd = e4m3.decode(q[t])
+        for hh in range(h):
+            sig = None if sink is None else float(np.float32(c * float(sink[hh]) * LOG2E))
+            out[n, hh], max_logit[n, hh], lse[n, hh] = emulate_row(
+                qd[hh], kk, vv, where // chunk, c_qk_log2, sig, kvs, p_format, limit, head, round_out)
     return out, max_logit, lse

@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 
 from fp8_block_sparse_gb300 import workloads as wl
-from oracle import attention as oa, emulate as em, index_topk as oi, quant as oq
+from oracle import attention as oa, emulate as em, index_topk as oi, mla as om, quant as oq
 
 BAR_ABS, BAR_REL, BAR_LSE = 4e-2, 1e-2, 2e-3
 
@@ -82,3 +82,24 @@ def test_single_e4m3_p_fails_the_relative_bar(tiny, decode, which):
     args = tiny if which == "tiny" else decode
     _, rel, _, _ = _errors(args, p_format="e4m3")
     assert rel > BAR_REL
+
+
+@pytest.fixture(scope="module")
+def mla():
+    w = wl.make_mla(wl.CONFIGS["mla"], T_override=6, S_override=3000, topk_override=512, len_range=(200, 512))
+    return (oq.quantize(w.q, w.scales["q"]), oq.quantize(w.kv, w.scales["kv"]), w.indices, w.topk_length,
+            w.sink, w.sm_scale, w.scales["q"], w.scales["kv"])
+
+
+def _mla_errors(args, **kw):
+    ref = om.sparse_mla(*args)
+    o, ml, lse = em.emulate_mla(*args, **kw)
+    return (np.abs(o - ref[0]).max(), np.linalg.norm(o - ref[0]) / np.linalg.norm(ref[0]),
+            np.abs(lse - ref[2]).max(), np.abs(ml - ref[1]).max())
+
+
+def test_mla_emulation_fp32_is_the_oracle_and_f16_is_inside_the_bars(mla):
+    err, rel, lerr, merr = _mla_errors(mla, p_format="fp32", round_out=False)
+    assert rel < 1e-6 and lerr < 1e-5 and merr < 1e-5, (err, rel, lerr, merr)
+    err, rel, lerr, _ = _mla_errors(mla)
+    assert err <= BAR_ABS and rel <= BAR_REL and lerr <= BAR_LSE
