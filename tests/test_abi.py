@@ -159,3 +159,17 @@ def test_rope_quant_validation(lib):
     # rows = 0: OK without reading any pointer
     assert lib.msa_rope_quant_fp8(null, null, 0, 0, 2, 128, 64, 0, 0, 0, 0, null, 1, null, 1,
                                   None, null, null) == 0
+
+
+def test_header_is_plain_c99():
+    # the boundary is a C ABI: the header must compile as strict C99 on its own
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    src = '#include "msa.h"\nint main(void) { return (int)MSA_OK; }\n'
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                        "-I", os.path.join(ROOT, "include"), "-fsyntax-only", "-x", "c", "-"],
+                       input=src, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
