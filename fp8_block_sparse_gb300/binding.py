@@ -204,6 +204,12 @@ def kv_store_fp8(page_table: torch.Tensor, seq_lens: torch.Tensor, cu_q: torch.T
             _dev(c, n, torch.uint8)
     kv = k if k is not None else v
     T = given[0].shape[0]
+    if any(x.shape[0] != T for x in given):
+        raise MsaError(1, "k, v and idx_k must have the same number of tokens")
+    if kv is not None and (kv.dim() != 3 or (k is not None and v is not None and k.shape != v.shape)):
+        raise MsaError(1, "k and v must be [T, Hkv, D] of one shape")
+    if idx_k is not None and idx_k.dim() != 2:
+        raise MsaError(1, "idx_k must be [T, d_idx]")
     Hkv, D = (kv.shape[1], kv.shape[2]) if kv is not None else (0, 16)
     d_idx = idx_k.shape[1] if idx_k is not None else 16
     parts = [(x, c, n, shape) for x, c, n, shape in

@@ -145,6 +145,10 @@ def test_kv_store_marshalling(fake):
         bd.kv_store_fp8(pt, sl, cu, kc, None, None, k=fused[:, :Hkv * D * 2:2].view(T, Hkv, D))
     with pytest.raises(bd.MsaError):                      # mixed dtypes
         bd.kv_store_fp8(pt, sl, cu, kc, vc, None, k=k, v=v.to(torch.float16))
+    with pytest.raises(bd.MsaError):                      # index K for fewer tokens
+        bd.kv_store_fp8(pt, sl, cu, kc, vc, ic, k=k, v=v, idx_k=ik[:T - 1])
+    with pytest.raises(bd.MsaError):                      # V with another head count
+        bd.kv_store_fp8(pt, sl, cu, kc, vc, None, k=k, v=v[:, :1])
 
 
 def test_rope_quant_marshalling(fake):
