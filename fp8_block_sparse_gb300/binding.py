@@ -8,6 +8,7 @@ library's CUDA kernels; when the library is missing, every call raises.
 
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 from typing import Optional
@@ -44,6 +45,7 @@ _SIGNATURES = {
     "msa_last_error_string": ([], ctypes.c_char_p),
     "msa_check_errors": ([_P], _I),
     "msa_profile_enable": ([_I], _I),
+    "msa_debug_force_timeouts": ([_I], _I),
     "msa_profile_last_ms": ([_FP], _I),
     "msa_quant_fp8": ([_P, _I, _I64, _I64, _I64, _P, _I, _I64, _FP, _P], _I),
     "msa_kv_store_fp8": ([_P, _P, _P, _I, _I64, _I64, _I64, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
@@ -92,8 +94,30 @@ def _scale(s: Optional[float]):
     return None if s is None else ctypes.pointer(ctypes.c_float(float(s)))
 
 
-def _stream(stream: Optional[torch.cuda.Stream]):
-    s = stream if stream is not None else torch.cuda.current_stream()
+def _device(*tensors) -> torch.device:
+    """The one device every given tensor (None entries skipped) lives on. A
+    call whose tensors sit on different GPUs is refused: the library would
+    launch on one device with another device's pointers."""
+    devs = {t.device for t in tensors if t is not None}
+    if len(devs) != 1:
+        raise MsaError(1, f"all tensors must be on one device, got {sorted(str(d) for d in devs)}")
+    return next(iter(devs))
+
+
+def _on(dev: torch.device):
+    """Makes `dev` the current device for the call (the library launches on
+    the current device, and looks up per-device state there)."""
+    return torch.cuda.device(dev) if dev.type == "cuda" else contextlib.nullcontext()
+
+
+def _stream(stream: Optional[torch.cuda.Stream], dev: Optional[torch.device] = None):
+    """The launch stream: the given one (which must belong to `dev`), else
+    torch's current stream of `dev` (of the current device when None)."""
+    if stream is not None:
+        if dev is not None and dev.type == "cuda" and stream.device != dev:
+            raise MsaError(1, f"stream is on {stream.device}, the tensors on {dev}")
+        return ctypes.c_void_p(stream.cuda_stream)
+    s = torch.cuda.current_stream(dev) if dev is not None else torch.cuda.current_stream()
     return ctypes.c_void_p(s.cuda_stream)
 
 
@@ -127,8 +151,19 @@ def _batch(page_table: torch.Tensor, seq_lens: torch.Tensor, cu_q: torch.Tensor)
 
 
 def check_errors(stream: Optional[torch.cuda.Stream] = None) -> None:
-    """Synchronise and raise if a kernel recorded a device-side data error."""
-    _check(load().msa_check_errors(_stream(stream)))
+    """Synchronise and raise if a kernel recorded a device-side data error
+    (on the stream's device, or the current device when no stream is given)."""
+    dev = stream.device if stream is not None else None
+    with (_on(dev) if dev is not None else contextlib.nullcontext()):
+        _check(load().msa_check_errors(_stream(stream, dev)))
+
+
+def debug_force_timeouts(on: bool) -> None:
+    """Debug switch of the current device: while on, every bounded wait in the
+    library's kernels that is not complete at its first test gives up at once
+    (the failure path: error word, drain, return). Outputs are meaningless
+    meanwhile; the next check_errors reports the timeout."""
+    _check(load().msa_debug_force_timeouts(1 if on else 0))
 
 
 def profile_enable(on: bool = True) -> None:
@@ -162,9 +197,11 @@ def quant_fp8(x: torch.Tensor, scale: Optional[float] = None, out: Optional[torc
     if out.numel() != x.numel():
         raise MsaError(1, f"out must hold {x.numel()} elements, got {out.numel()}")
     o2 = out.view(rows, cols)
-    _check(lib.msa_quant_fp8(_ptr(x2), MSA_BF16 if x.dtype == torch.bfloat16 else MSA_FP16,
-                             rows, cols, x2.stride(0) if rows else cols, _ptr(o2), MSA_E4M3,
-                             o2.stride(0) if rows else cols, _scale(scale), _stream(stream)))
+    dev = _device(x, out)
+    with _on(dev):
+        _check(lib.msa_quant_fp8(_ptr(x2), MSA_BF16 if x.dtype == torch.bfloat16 else MSA_FP16,
+                                 rows, cols, x2.stride(0) if rows else cols, _ptr(o2), MSA_E4M3,
+                                 o2.stride(0) if rows else cols, _scale(scale), _stream(stream, dev)))
     return out
 
 
@@ -221,13 +258,16 @@ def kv_store_fp8(page_table: torch.Tensor, seq_lens: torch.Tensor, cu_q: torch.T
     for _, c, n, shape in parts:
         if tuple(c.shape[1:]) != shape or c.shape[0] != cache.shape[0]:
             raise MsaError(1, f"{n} must be [num_pages, {', '.join(map(str, shape))}], got {tuple(c.shape)}")
-    _check(lib.msa_kv_store_fp8(_ptr(k), _ptr(v), _ptr(idx_k),
-                                MSA_BF16 if dt == torch.bfloat16 else MSA_FP16,
-                                _token_rows(k, "k", Hkv * D), _token_rows(v, "v", Hkv * D),
-                                _token_rows(idx_k, "idx_k", d_idx), _ptr(page_table), _ptr(seq_lens),
-                                _ptr(cu_q), B, T, max_pages, cache.shape[0], Hkv, D, d_idx,
-                                _scale(k_scale), _scale(v_scale), _scale(idx_k_scale),
-                                _ptr(k_cache), _ptr(v_cache), _ptr(idx_k_cache), _stream(stream)))
+    dev = _device(k, v, idx_k, k_cache, v_cache, idx_k_cache, page_table, seq_lens, cu_q)
+    with _on(dev):
+        _check(lib.msa_kv_store_fp8(_ptr(k), _ptr(v), _ptr(idx_k),
+                                    MSA_BF16 if dt == torch.bfloat16 else MSA_FP16,
+                                    _token_rows(k, "k", Hkv * D), _token_rows(v, "v", Hkv * D),
+                                    _token_rows(idx_k, "idx_k", d_idx), _ptr(page_table),
+                                    _ptr(seq_lens), _ptr(cu_q), B, T, max_pages, cache.shape[0], Hkv,
+                                    D, d_idx, _scale(k_scale), _scale(v_scale), _scale(idx_k_scale),
+                                    _ptr(k_cache), _ptr(v_cache), _ptr(idx_k_cache),
+                                    _stream(stream, dev)))
 
 
 def rope_quant_fp8(nope: Optional[torch.Tensor], pe: torch.Tensor, cos_sin_cache: torch.Tensor,
@@ -261,10 +301,13 @@ def rope_quant_fp8(nope: Optional[torch.Tensor], pe: torch.Tensor, cos_sin_cache
         raise MsaError(1, f"out must be [{rows}, {heads}, {d_nope + d_rope}]")
     ns = (nope.stride(0), nope.stride(1)) if nope is not None else (0, 0)
     ps = (pe.stride(0), pe.stride(1) if hp == heads and heads > 1 else 0)
-    _check(lib.msa_rope_quant_fp8(_ptr(nope), _ptr(pe), MSA_BF16 if dt == torch.bfloat16 else MSA_FP16,
-                                  rows, heads, d_nope, d_rope, ns[0], ns[1], ps[0], ps[1],
-                                  _ptr(cos_sin_cache), cos_sin_cache.shape[0], _ptr(positions),
-                                  1 if is_neox else 0, _scale(scale), _ptr(out), _stream(stream)))
+    dev = _device(nope, pe, cos_sin_cache, positions, out)
+    with _on(dev):
+        _check(lib.msa_rope_quant_fp8(_ptr(nope), _ptr(pe), MSA_BF16 if dt == torch.bfloat16 else MSA_FP16,
+                                      rows, heads, d_nope, d_rope, ns[0], ns[1], ps[0], ps[1],
+                                      _ptr(cos_sin_cache), cos_sin_cache.shape[0], _ptr(positions),
+                                      1 if is_neox else 0, _scale(scale), _ptr(out),
+                                      _stream(stream, dev)))
     return out
 
 
@@ -290,9 +333,12 @@ def index_topk(idx_q: torch.Tensor, idx_k_cache: torch.Tensor, page_table: torch
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=idx_q.device)
     _dev(workspace, "workspace", torch.uint8)
-    _check(lib.msa_index_topk(_ptr(idx_q), _ptr(idx_k_cache), _ptr(page_table), _ptr(seq_lens),
-                              _ptr(cu_q), B, T, max_q_len, Hidx, D, topk, num_pages, max_pages,
-                              _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)))
+    dev = _device(idx_q, idx_k_cache, page_table, seq_lens, cu_q, out, workspace)
+    with _on(dev):
+        _check(lib.msa_index_topk(_ptr(idx_q), _ptr(idx_k_cache), _ptr(page_table), _ptr(seq_lens),
+                                  _ptr(cu_q), B, T, max_q_len, Hidx, D, topk, num_pages, max_pages,
+                                  _ptr(out), _ptr(workspace), workspace.numel(),
+                                  _stream(stream, dev)))
     return out
 
 
@@ -310,9 +356,11 @@ def index_topk_noalloc(idx_q: torch.Tensor, idx_k_cache: torch.Tensor, page_tabl
     if out is None:
         out = torch.empty((Hidx, T, topk), dtype=torch.int32, device=idx_q.device)
     _dev(out, "out", torch.int32, (Hidx, T, topk))
-    _check(lib.msa_index_topk_noalloc(_ptr(idx_q), _ptr(idx_k_cache), _ptr(page_table), _ptr(seq_lens),
-                                      _ptr(cu_q), B, T, max_q_len, Hidx, D, topk, num_pages, max_pages,
-                                      _ptr(out), _stream(stream)))
+    dev = _device(idx_q, idx_k_cache, page_table, seq_lens, cu_q, out)
+    with _on(dev):
+        _check(lib.msa_index_topk_noalloc(_ptr(idx_q), _ptr(idx_k_cache), _ptr(page_table),
+                                          _ptr(seq_lens), _ptr(cu_q), B, T, max_q_len, Hidx, D, topk,
+                                          num_pages, max_pages, _ptr(out), _stream(stream, dev)))
     return out
 
 
@@ -352,12 +400,15 @@ def sparse_attn_fwd(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tenso
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
     _dev(workspace, "workspace", torch.uint8)
-    _check(lib.msa_sparse_attn_fwd(
-        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table), _ptr(seq_lens), _ptr(cu_q),
-        _ptr(topk_indices), _ptr(sink), float(sm_scale), _scale(q_scale), _scale(k_scale),
-        _scale(v_scale), B, T, max_q_len, Hq, Hkv, Hidx, D, topk, num_pages, max_pages,
-        _ptr(out), _ptr(max_logit), _ptr(lse), _ptr(workspace), workspace.numel(),
-        _stream(stream)))
+    dev = _device(q, k_cache, v_cache, page_table, seq_lens, cu_q, topk_indices, sink, out,
+                  max_logit, lse, workspace)
+    with _on(dev):
+        _check(lib.msa_sparse_attn_fwd(
+            _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(page_table), _ptr(seq_lens), _ptr(cu_q),
+            _ptr(topk_indices), _ptr(sink), float(sm_scale), _scale(q_scale), _scale(k_scale),
+            _scale(v_scale), B, T, max_q_len, Hq, Hkv, Hidx, D, topk, num_pages, max_pages,
+            _ptr(out), _ptr(max_logit), _ptr(lse), _ptr(workspace), workspace.numel(),
+            _stream(stream, dev)))
     return out, max_logit, lse
 
 
@@ -386,8 +437,10 @@ def sparse_mla_fwd(q: torch.Tensor, kv: torch.Tensor, indices: torch.Tensor,
     _dev(out, "out", torch.bfloat16, (T, H, d_v))
     _dev(max_logits, "max_logits", torch.float32, (T, H))
     _dev(lse, "lse", torch.float32, (T, H))
-    _check(lib.msa_sparse_mla_fwd(_ptr(q), _ptr(kv), _ptr(indices), _ptr(topk_length), _ptr(sink),
-                                  float(sm_scale), _scale(q_scale), _scale(kv_scale), T, H, S_kv,
-                                  d_qk, d_v, topk, _ptr(out), _ptr(max_logits), _ptr(lse),
-                                  _stream(stream)))
+    dev = _device(q, kv, indices, topk_length, sink, out, max_logits, lse)
+    with _on(dev):
+        _check(lib.msa_sparse_mla_fwd(_ptr(q), _ptr(kv), _ptr(indices), _ptr(topk_length), _ptr(sink),
+                                      float(sm_scale), _scale(q_scale), _scale(kv_scale), T, H, S_kv,
+                                      d_qk, d_v, topk, _ptr(out), _ptr(max_logits), _ptr(lse),
+                                      _stream(stream, dev)))
     return out, max_logits, lse

@@ -15,7 +15,7 @@
 
 namespace msa {
 
-__device__ unsigned g_msa_error_word;
+__device__ DeviceState g_msa_state;
 
 namespace {
 
@@ -73,8 +73,8 @@ unsigned* device_error_word() {
   std::lock_guard<std::mutex> lock(g_mutex);
   if (g_err_ptr[d] == nullptr) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_msa_error_word) != cudaSuccess) return nullptr;
-    g_err_ptr[d] = static_cast<unsigned*>(p);
+    if (cudaGetSymbolAddress(&p, g_msa_state) != cudaSuccess) return nullptr;
+    g_err_ptr[d] = &static_cast<DeviceState*>(p)->err;
   }
   return g_err_ptr[d];
 }
@@ -143,6 +143,23 @@ bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank, co
   return true;
 }
 
+msa_status check_index_topk_sizes(const char* fn, int B, int T, int max_q_len, int Hidx, int D,
+                                  int topk, int num_pages, int max_pages) {
+  if (B < 1 || T < 0 || Hidx < 1 || num_pages < 1 || max_pages < 1)
+    return fail(MSA_ERR_INVALID_ARG, std::string(fn) + ": bad B/T/Hidx/num_pages/max_pages");
+  if (T > 0 && (max_q_len < 1 || max_q_len > T))
+    return fail(MSA_ERR_INVALID_ARG, std::string(fn) + ": max_q_len must be in [1, T]");
+  if (D != 64 && D != 128)
+    return fail(MSA_ERR_UNSUPPORTED, std::string(fn) + ": index head dim must be 64 or 128");
+  if (topk < 1 || topk > 64)
+    return fail(MSA_ERR_UNSUPPORTED, std::string(fn) + ": topk must be in [1, 64]");
+  if (Hidx > 16 || (Hidx & (Hidx - 1)) != 0)
+    return fail(MSA_ERR_UNSUPPORTED, std::string(fn) + ": Hidx must be a power of two <= 16");
+  if (max_pages > 2048)
+    return fail(MSA_ERR_UNSUPPORTED, std::string(fn) + ": max_pages must be <= 2048");
+  return MSA_OK;
+}
+
 }  // namespace msa
 
 using namespace msa;
@@ -182,6 +199,16 @@ msa_status msa_check_errors(msa_stream_t stream) {
   if (word & MSA_DEVERR_TIMEOUT) return fail(MSA_ERR_TIMEOUT, "a device wait ran out its limit");
   if (word & MSA_DEVERR_DATA)
     return fail(MSA_ERR_DATA, "a kernel saw a page id or index outside its valid range");
+  return MSA_OK;
+}
+
+msa_status msa_debug_force_timeouts(int on) {
+  unsigned* p = device_error_word();
+  if (p == nullptr) return fail(MSA_ERR_CUDA, "msa_debug_force_timeouts: no device state");
+  const unsigned v = on ? 1u : 0u;
+  DeviceState* st = reinterpret_cast<DeviceState*>(p);
+  const cudaError_t e = cudaMemcpy(&st->force_timeouts, &v, sizeof(v), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(e, "msa_debug_force_timeouts");
   return MSA_OK;
 }
 
@@ -340,14 +367,8 @@ msa_status msa_index_topk(const uint8_t* idx_q, const uint8_t* idx_k_cache,
                           int max_pages, int32_t* topk_indices, void* workspace,
                           size_t workspace_bytes, msa_stream_t stream) {
   const char* fn = "msa_index_topk";
-  if (B < 1 || T < 0 || Hidx < 1 || num_pages < 1 || max_pages < 1)
-    return fail(MSA_ERR_INVALID_ARG, std::string(fn) + ": bad B/T/Hidx/num_pages/max_pages");
-  if (T > 0 && (max_q_len < 1 || max_q_len > T))
-    return fail(MSA_ERR_INVALID_ARG, std::string(fn) + ": max_q_len must be in [1, T]");
-  if (D != 64 && D != 128)
-    return fail(MSA_ERR_UNSUPPORTED, std::string(fn) + ": index head dim must be 64 or 128");
-  if (topk < 1 || topk > 64)
-    return fail(MSA_ERR_UNSUPPORTED, std::string(fn) + ": topk must be in [1, 64]");
+  const msa_status st = check_index_topk_sizes(fn, B, T, max_q_len, Hidx, D, topk, num_pages, max_pages);
+  if (st != MSA_OK) return st;
   if (T == 0) return MSA_OK;
   if (!idx_q || !idx_k_cache || !page_table || !seq_lens || !cu_q || !topk_indices)
     return fail(MSA_ERR_INVALID_ARG, std::string(fn) + ": null pointer");

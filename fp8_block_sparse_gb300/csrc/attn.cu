@@ -115,7 +115,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   __shared__ uint64_t bar_q, bar_kf[kStages], bar_ke[kStages], bar_vf[kStages], bar_ve[kStages],
-      bar_sf[2], bar_pf[2], bar_done;
+      bar_sf[2], bar_pf[2], bar_done, bar_drain;
   __shared__ uint32_t tmem_base_s;
   __shared__ int n_union_s;
   __shared__ int abort_s;
@@ -134,7 +134,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 
   if (tid < 64) sBits[tid] = 0u;
   if (tid == 0) {
-    abort_s = 0;
+    abort_s = initial_abort(err);
     mbar_init(&bar_q, 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bar_kf[s], 1); mbar_init(&bar_ke[s], 1);
@@ -142,6 +142,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     }
     for (int x = 0; x < 2; ++x) { mbar_init(&bar_sf[x], 1); mbar_init(&bar_pf[x], 4); }
     mbar_init(&bar_done, 1);
+    mbar_init(&bar_drain, 1);
     fence_barrier_init();
   }
   if (warp == 1) { tmem_alloc(&tmem_base_s, 512); tmem_relinquish(); }
@@ -212,6 +213,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       tma_load_3d(smem + kQOff, &tm_q, &bar_q, 0, g * G, ti.t0);
       tma_load_3d(smem + kQOff + 16384, &tm_q, &bar_q, 0, g * G, ti.t0 + toks);
       const int32_t* prow = page_table + size_t(ti.b) * max_pages;
+      int nk = 0, nv = 0;                                  // copies issued per ring
       for (int j = 0; j < nU; ++j) {
         const int s = j % kStages;
         const uint32_t ph = ((j / kStages) & 1) ^ 1;
@@ -221,12 +223,19 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         if (!mbar_wait_ab(&bar_ke[s], ph, err, &abort_s)) break;
         mbar_arrive_expect_tx(&bar_kf[s], 16384);
         tma_load_2d(smem + kKOff + s * 16384, &tm_k, &bar_kf[s], 0, (page * Hkv + g) * 128);
+        ++nk;
         if (!mbar_wait_ab(&bar_ve[s], ph, err, &abort_s)) break;
         mbar_arrive_expect_tx(&bar_vf[s], 32768);
         bulk_load(smem + kVOff + s * 32768,
                   vt_img + ((size_t(ti.b) * max_pages + blk) * Hkv + g) * 32768, 32768, &bar_vf[s]);
+        ++nv;
       }
-    } else if (warp == 1 && nU > 0 && mbar_wait_warp(&bar_q, 0, err, &abort_s)) {
+      // exit-path drain (a no-op unless a wait gave up): every copy has landed
+      mbar_wait(&bar_q, 0, err);
+      mbar_drain_ring(bar_kf, kStages, nk, err);
+      mbar_drain_ring(bar_vf, kStages, nv, err);
+    } else if (warp == 1 && nU > 0) {
+     if (mbar_wait_warp(&bar_q, 0, err, &abort_s)) {
       // ---------------- MMA issue (whole warp, one elected lane per instruction)
       const uint32_t sq = smem_addr(smem + kQOff);
       auto issue_s = [&](int j, int x) -> bool {
@@ -260,6 +269,8 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         }
         if (ok && j == nU - 1) mma_commit_w(&bar_done);
       }
+     }
+      mma_drain_w(&bar_drain, err);          // no MMA in flight once TMEM is freed
     }
   } else {
     setmaxnreg_inc<224>();
@@ -468,7 +479,8 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   __shared__ uint64_t bar_q, bar_kf[kDecKStages], bar_ke[kDecKStages], bar_vf[kDecVStages],
-      bar_ve[kDecVStages], bar_sf[2], bar_se[2], bar_pf[2], bar_pe[2], bar_pv, bar_done, bar_vt;
+      bar_ve[kDecVStages], bar_sf[2], bar_se[2], bar_pf[2], bar_pe[2], bar_pv, bar_done, bar_vt,
+      bar_drain;
   __shared__ uint32_t tmem_base_s;
   __shared__ int n_union_s;
   __shared__ int abort_s;
@@ -550,8 +562,9 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
   const int j0 = c * cs, n = min(nU, j0 + cs) - j0;
 
   if (tid == 0) {
-    abort_s = 0;
+    abort_s = initial_abort(err);
     mbar_init(&bar_q, 1);
+    mbar_init(&bar_drain, 1);
     for (int s = 0; s < kDecKStages; ++s) { mbar_init(&bar_kf[s], 1); mbar_init(&bar_ke[s], 1); }
     for (int s = 0; s < kDecVStages; ++s) { mbar_init(&bar_vf[s], 1); mbar_init(&bar_ve[s], 1); }
     for (int s = 0; s < 2; ++s) {
@@ -579,6 +592,7 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     }
     const int32_t* prow = page_table + size_t(b) * max_pages;
     const int tail_blk = (L - 1) >> 7, tail_rows = L - tail_blk * 128;
+    int nk = 0, nv = 0, nvt = 0;                    // phases armed per ring (lane 0's copies)
     for (int jj = 0; jj < n; ++jj) {
       const int s = jj % kDecKStages, sv = jj % kDecVStages;
       const uint32_t ph = ((jj / kDecKStages) & 1) ^ 1, phv = ((jj / kDecVStages) & 1) ^ 1;
@@ -596,6 +610,7 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         if (ok) {
           mbar_arrive_expect_tx(&bar_kf[s], 16384);
           tma_load_2d(smem + kDKOff + s * 16384, &tm_k, &bar_kf[s], 0, row0);
+          ++nk;
           ok = mbar_wait_ab(&bar_ve[sv], phv, err, &abort_s);
         }
       }
@@ -604,8 +619,9 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         if (lane == 0) {
           mbar_arrive_expect_tx(&bar_vt, 16384);
           tma_load_2d(vs, &tm_v, &bar_vt, 0, row0);
+          nvt = 1;
         }
-        if (!mbar_wait_ab(&bar_vt, 0, err, &abort_s)) break;
+        if (!mbar_wait_warp(&bar_vt, 0, err, &abort_s)) break;
         uint4* rows = reinterpret_cast<uint4*>(vs + tail_rows * 128);   // swizzle stays inside a row
         for (int x = lane; x < (128 - tail_rows) * 8; x += 32) rows[x] = make_uint4(0u, 0u, 0u, 0u);
         fence_async_shared();
@@ -615,6 +631,13 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         mbar_arrive_expect_tx(&bar_vf[sv], 16384);
         tma_load_2d(vs, &tm_v, &bar_vf[sv], 0, row0);
       }
+      ++nv;
+    }
+    if (lane == 0) {            // exit-path drain (a no-op unless a wait gave up)
+      mbar_wait(&bar_q, 0, err);
+      mbar_drain_ring(bar_kf, kDecKStages, nk, err);
+      mbar_drain_ring(bar_vf, kDecVStages, nv, err);
+      if (nvt) mbar_wait(&bar_vt, 0, err);
     }
   } else if (warp == 1) {
     if (mbar_wait_warp(&bar_q, 0, err, &abort_s)) {        // whole warp, elected issue
@@ -656,6 +679,7 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         if (jj == n - 1) mma_commit_w(&bar_done);
       }
     }
+    mma_drain_w(&bar_drain, err);            // no MMA in flight once TMEM is freed
   } else {
     // ---------------- softmax: thread = key lane of S^T and d lane of O^T,
     // query rows r0 .. r0+RPT-1

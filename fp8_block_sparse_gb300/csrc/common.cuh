@@ -74,6 +74,18 @@ MSA_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* err) {
   }
 }
 
+// Values of a CTA's shared abort flag: 0 = run; 1 = some wait of this CTA
+// ran out, every role stops waiting; kAbortForced = the device's debug switch
+// that forces timeouts is on: the first wait that is not complete at its
+// first test gives up at once (then the flag becomes 1).
+constexpr int kAbortForced = 2;
+
+// The initial value of a CTA's abort flag (read once, at kernel start, from
+// the per-device state that `err` points into).
+MSA_DEV int initial_abort(const unsigned* err) {
+  return reinterpret_cast<const volatile DeviceState*>(err)->force_timeouts ? kAbortForced : 0;
+}
+
 // As mbar_wait, but returns false at once when *abort is set, and sets it
 // when its own limit runs out: after the first timeout every role of the CTA
 // stops waiting and drains its loop quickly.
@@ -81,7 +93,14 @@ MSA_DEV bool mbar_wait_ab(uint64_t* bar, uint32_t parity, unsigned* err, volatil
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    if (*abort) return false;
+    const int ab = *abort;
+    if (ab) {
+      if (ab == kAbortForced) {
+        atomicOr(err, MSA_DEVERR_TIMEOUT);
+        *abort = 1;
+      }
+      return false;
+    }
     for (int i = 0; i < 256; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (globaltimer_ns() - t0 > kWaitLimitNs) {
@@ -89,6 +108,18 @@ MSA_DEV bool mbar_wait_ab(uint64_t* bar, uint32_t parity, unsigned* err, volatil
       *abort = 1;
       return false;
     }
+  }
+}
+
+// Exit-path drain of a ring of `stages` barriers whose iterations 0..n-1 were
+// each armed with an asynchronous copy (or completed by an arrival): waits,
+// with the fixed limit and regardless of the abort flag, for the last armed
+// phase of every stage. Phases of one barrier complete in order, so after
+// this no copy issued into the ring is still writing shared memory.
+MSA_DEV void mbar_drain_ring(uint64_t* bars, int stages, int n, unsigned* err) {
+  for (int s = 0; s < stages && s < n; ++s) {
+    const int j = s + ((n - 1 - s) / stages) * stages;       // last iteration on stage s
+    mbar_wait(&bars[s], uint32_t((j / stages) & 1), err);
   }
 }
 
@@ -327,6 +358,13 @@ MSA_DEV void mma_commit_w(uint64_t* bar) {
           smem_addr(bar))
       : "memory");
 }
+// Exit-path drain of the MMA-issuing warp (whole warp, converged): commits
+// every tcgen05 operation it issued to `bar` (a barrier of count 1 used for
+// nothing else) and waits for it with the fixed limit, regardless of the
+// abort flag, so no MMA still reads shared memory or writes TMEM once the CTA
+// frees them.
+MSA_DEV void mma_drain_w(uint64_t* bar, unsigned* err);
+
 // mbar_wait for a whole converged warp; the result is the same in every lane.
 MSA_DEV bool mbar_wait_warp(uint64_t* bar, uint32_t parity, unsigned* err) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, err));
@@ -334,6 +372,11 @@ MSA_DEV bool mbar_wait_warp(uint64_t* bar, uint32_t parity, unsigned* err) {
 // mbar_wait_ab for a whole converged warp; the result is the same in every lane.
 MSA_DEV bool mbar_wait_warp(uint64_t* bar, uint32_t parity, unsigned* err, volatile int* abort) {
   return __all_sync(0xffffffffu, mbar_wait_ab(bar, parity, err, abort));
+}
+
+MSA_DEV void mma_drain_w(uint64_t* bar, unsigned* err) {
+  mma_commit_w(bar);
+  mbar_wait_warp(bar, 0, err);
 }
 
 // ---------------------------------------------------------------- misc

@@ -66,8 +66,10 @@ index_score_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
   using L = PrefillSmem<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t bar_q, bar_full[kStages], bar_empty[kStages], bar_tfull[2], bar_tempty[2];
+  __shared__ uint64_t bar_q, bar_full[kStages], bar_empty[kStages], bar_tfull[2], bar_tempty[2],
+      bar_drain;
   __shared__ uint32_t tmem_base_s;
+  __shared__ int abort_s;
 
   const int n_tiles = *n_tiles_p;
   const int tile_rank = blockIdx.x / chunks_per_tile;
@@ -86,7 +88,9 @@ index_score_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
   float* sScore = reinterpret_cast<float*>(smem + L::kScore);
 
   if (tid == 0) {
+    abort_s = initial_abort(err);
     mbar_init(&bar_q, 1);
+    mbar_init(&bar_drain, 1);
     for (int s = 0; s < kStages; ++s) { mbar_init(&bar_full[s], 1); mbar_init(&bar_empty[s], 1); }
     for (int s = 0; s < 2; ++s) { mbar_init(&bar_tfull[s], 1); mbar_init(&bar_tempty[s], 4); }
     fence_barrier_init();
@@ -103,21 +107,26 @@ index_score_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
       mbar_arrive_expect_tx(&bar_q, 128 * D);
       tma_load_2d(sQ, &tm_q, &bar_q, 0, ti.t0 * Hidx);
       const int32_t* prow = page_table + size_t(ti.b) * max_pages;
+      int nk = 0;
       for (int j = 0; j < nblk; ++j) {
         const int s = j % kStages;
-        if (!mbar_wait(&bar_empty[s], ((j / kStages) & 1) ^ 1, err)) break;
+        if (!mbar_wait_ab(&bar_empty[s], ((j / kStages) & 1) ^ 1, err, &abort_s)) break;
         int page = __ldg(prow + c0 + j);
         if (page < 0 || page >= num_pages) { atomicOr(err, MSA_DEVERR_DATA); page = 0; }
         mbar_arrive_expect_tx(&bar_full[s], 128 * D);
         tma_load_2d(sK + s * 16384, &tm_k, &bar_full[s], 0, page * 128);
+        ++nk;
       }
+      // exit-path drain (a no-op unless a wait gave up): every copy has landed
+      mbar_wait(&bar_q, 0, err);
+      mbar_drain_ring(bar_full, kStages, nk, err);
     }
   } else if (warp == 1) {
-    if (mbar_wait_warp(&bar_q, 0, err)) {          // whole warp, elected issue
+    if (mbar_wait_warp(&bar_q, 0, err, &abort_s)) {          // whole warp, elected issue
       for (int j = 0; j < nblk; ++j) {
         const int s = j % kStages, buf = j & 1;
-        if (!mbar_wait_warp(&bar_full[s], (j / kStages) & 1, err)) break;
-        if (!mbar_wait_warp(&bar_tempty[buf], ((j >> 1) & 1) ^ 1, err)) break;
+        if (!mbar_wait_warp(&bar_full[s], (j / kStages) & 1, err, &abort_s)) break;
+        if (!mbar_wait_warp(&bar_tempty[buf], ((j >> 1) & 1) ^ 1, err, &abort_s)) break;
         tc_fence_after();
         const uint32_t aq = smem_addr(sQ), bk = smem_addr(sK + s * 16384);
 #pragma unroll
@@ -128,12 +137,13 @@ index_score_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
         mma_commit_w(&bar_tfull[buf]);
       }
     }
+    mma_drain_w(&bar_drain, err);            // no MMA in flight once TMEM is freed
   } else {
     // epilogue: warps 2..5 own TMEM lanes 32*(warp%4) .. +31
     const int row = (warp & 3) * 32 + lane;
     for (int j = 0; j < nblk; ++j) {
       const int buf = j & 1;
-      if (!mbar_wait(&bar_tfull[buf], (j >> 1) & 1, err)) break;
+      if (!mbar_wait_warp(&bar_tfull[buf], (j >> 1) & 1, err, &abort_s)) break;   // uniform
       tc_fence_after();
       float m = -INFINITY;
 #pragma unroll
@@ -179,8 +189,10 @@ index_score_decode_kernel(const __grid_constant__ CUtensorMap tm_q,
   constexpr uint32_t kIdesc = idesc_f32(128, 16);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t bar_q, bar_full[kStages], bar_empty[kStages], bar_tfull[kBufs], bar_tempty[kBufs];
+  __shared__ uint64_t bar_q, bar_full[kStages], bar_empty[kStages], bar_tfull[kBufs], bar_tempty[kBufs],
+      bar_drain;
   __shared__ uint32_t tmem_base_s;
+  __shared__ int abort_s;
   __shared__ uint32_t sred[kChunk][16];   // order-preserving keys of the block maxima
 
   const int t = blockIdx.x / chunks_per_tok;
@@ -201,7 +213,9 @@ index_score_decode_kernel(const __grid_constant__ CUtensorMap tm_q,
   uint8_t* sQ = smem + kStages * 16384;     // 16 rows x D
 
   if (tid == 0) {
+    abort_s = initial_abort(err);
     mbar_init(&bar_q, 1);
+    mbar_init(&bar_drain, 1);
     for (int s = 0; s < kStages; ++s) { mbar_init(&bar_full[s], 1); mbar_init(&bar_empty[s], 1); }
     for (int s = 0; s < kBufs; ++s) { mbar_init(&bar_tfull[s], 1); mbar_init(&bar_tempty[s], 4); }
     fence_barrier_init();
@@ -216,21 +230,26 @@ index_score_decode_kernel(const __grid_constant__ CUtensorMap tm_q,
       mbar_arrive_expect_tx(&bar_q, 16 * D);
       tma_load_2d(sQ, &tm_q, &bar_q, 0, t * Hidx);
       const int32_t* prow = page_table + size_t(b) * max_pages;
+      int nk = 0;
       for (int j = 0; j < nblk; ++j) {
         const int s = j % kStages;
-        if (!mbar_wait(&bar_empty[s], ((j / kStages) & 1) ^ 1, err)) break;
+        if (!mbar_wait_ab(&bar_empty[s], ((j / kStages) & 1) ^ 1, err, &abort_s)) break;
         int page = __ldg(prow + c0 + j);
         if (page < 0 || page >= num_pages) { atomicOr(err, MSA_DEVERR_DATA); page = 0; }
         mbar_arrive_expect_tx(&bar_full[s], 128 * D);
         tma_load_2d(sK + s * 16384, &tm_k, &bar_full[s], 0, page * 128);
+        ++nk;
       }
+      // exit-path drain (a no-op unless a wait gave up): every copy has landed
+      mbar_wait(&bar_q, 0, err);
+      mbar_drain_ring(bar_full, kStages, nk, err);
     }
   } else if (warp == 1) {
-    if (mbar_wait_warp(&bar_q, 0, err)) {          // whole warp, elected issue
+    if (mbar_wait_warp(&bar_q, 0, err, &abort_s)) {          // whole warp, elected issue
       for (int j = 0; j < nblk; ++j) {
         const int s = j % kStages, buf = j % kBufs;
-        if (!mbar_wait_warp(&bar_full[s], (j / kStages) & 1, err)) break;
-        if (!mbar_wait_warp(&bar_tempty[buf], ((j / kBufs) & 1) ^ 1, err)) break;
+        if (!mbar_wait_warp(&bar_full[s], (j / kStages) & 1, err, &abort_s)) break;
+        if (!mbar_wait_warp(&bar_tempty[buf], ((j / kBufs) & 1) ^ 1, err, &abort_s)) break;
         tc_fence_after();
         const uint32_t ak = smem_addr(sK + s * 16384), bq = smem_addr(sQ);
 #pragma unroll
@@ -241,6 +260,7 @@ index_score_decode_kernel(const __grid_constant__ CUtensorMap tm_q,
         mma_commit_w(&bar_tfull[buf]);
       }
     }
+    mma_drain_w(&bar_drain, err);            // no MMA in flight once TMEM is freed
   } else {
     const int q4 = warp & 3;
     const int et = tid - 64;
@@ -248,7 +268,7 @@ index_score_decode_kernel(const __grid_constant__ CUtensorMap tm_q,
     asm volatile("bar.sync 1, 128;" ::: "memory");
     for (int j = 0; j < nblk; ++j) {
       const int buf = j % kBufs;
-      if (!mbar_wait(&bar_tfull[buf], (j / kBufs) & 1, err)) break;
+      if (!mbar_wait_warp(&bar_tfull[buf], (j / kBufs) & 1, err, &abort_s)) break;   // uniform
       tc_fence_after();
       uint32_t v[16];
       tmem_ld16(tmem_addr(tmem + buf * 16, q4 * 32, 0), v);

@@ -9,16 +9,26 @@
 
 #include <string>
 
+#include "msa.h"
+
 namespace msa {
 
 // Bits of the device error word.
 constexpr unsigned MSA_DEVERR_DATA = 1u;     // bad page id / index seen by a kernel
 constexpr unsigned MSA_DEVERR_TIMEOUT = 2u;  // a bounded wait gave up
 
+// Per-device state in the library image. Kernels get the address of `err`
+// (the first member) and find the rest through it.
+struct DeviceState {
+  unsigned err;              // MSA_DEVERR_* bits, cleared by msa_check_errors
+  unsigned force_timeouts;   // debug: nonzero makes every unfinished wait give up
+};
+
 // Sets the message msa_last_error_string() returns on this thread.
 void set_last_error(const std::string& msg);
 
-// Device address of this device's error word (set up once per device).
+// Device address of this device's error word, the first member of its
+// DeviceState (set up once per device).
 unsigned* device_error_word();
 
 // Builds a tiled TMA descriptor through the driver entry point. Returns false
@@ -86,6 +96,10 @@ struct IndexArgs {
   unsigned* err;
 };
 cudaError_t launch_index_topk(const IndexArgs& a, cudaStream_t stream, const char** why);
+// The scalar and support checks of msa_index_topk (every check that needs no
+// pointer), in its order; fills the last-error message and returns its status.
+msa_status check_index_topk_sizes(const char* fn, int B, int T, int max_q_len, int Hidx, int D,
+                                  int topk, int num_pages, int max_pages);
 size_t index_workspace_bytes(int T, int Hidx, int max_pages);
 
 // Step (c), GQA.

@@ -71,7 +71,7 @@ mla_prefill_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_con
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   __shared__ uint64_t bar_q, bar_kf[2], bar_ke[2], bar_sf[2], bar_se[2], bar_pf[2], bar_pe[2],
-      bar_vtf[2], bar_vte[2], bar_pv, bar_done;
+      bar_vtf[2], bar_vte[2], bar_pv, bar_done, bar_drain;
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_s;
 
@@ -83,8 +83,9 @@ mla_prefill_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_con
   const int32_t* idx_row = indices + size_t(t) * topk;
 
   if (tid == 0) {
-    abort_s = 0;
+    abort_s = initial_abort(err);
     mbar_init(&bar_q, 1);
+    mbar_init(&bar_drain, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bar_kf[s], 1); mbar_init(&bar_ke[s], 5);
       mbar_init(&bar_sf[s], 1); mbar_init(&bar_se[s], 4);
@@ -147,6 +148,10 @@ mla_prefill_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_con
           if (j == nch - 1) mma_commit_w(&bar_done);
         }
       }
+      // exit-path drain (a no-op unless a wait gave up): no MMA in flight and
+      // the Q copies landed once TMEM and shared memory are released
+      mma_drain_w(&bar_drain, err);
+      if (lane == 0) mbar_wait(&bar_q, 0, err);
     }
   } else if (warp <= 4) {
     // ---------------- gather warps: copy chunk j, then publish chunk j-1 once it has landed

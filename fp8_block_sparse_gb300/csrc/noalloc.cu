@@ -69,6 +69,12 @@ extern "C" msa_status msa_index_topk_noalloc(const uint8_t* idx_q, const uint8_t
                                              int Hidx, int D, int topk, int num_pages,
                                              int max_pages, int32_t* topk_indices,
                                              msa_stream_t stream) {
+  // msa_index_topk's own argument checks come first, so an invalid or
+  // unsupported call reports that and not the size of the fixed scratch
+  const msa_status st = msa::check_index_topk_sizes("msa_index_topk_noalloc", B, T, max_q_len, Hidx,
+                                                    D, topk, num_pages, max_pages);
+  if (st != MSA_OK) return st;
+  if (T == 0) return MSA_OK;
   const size_t need = msa_index_topk_workspace_size(T, Hidx, max_pages);
   if (need > msa::kNoAllocScratchBytes) {
     msa::set_last_error("msa_index_topk_noalloc: these sizes need " + std::to_string(need) +

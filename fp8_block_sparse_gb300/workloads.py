@@ -135,15 +135,27 @@ def amax_scale(bits: np.ndarray) -> float:
     return float(np.float32(amax) / np.float32(FP8_MAX))
 
 
-def redraw_rows(seed: int, tensor_name: str, attempt: int, n_rows: int, last: int,
-                dist_vector: Optional[np.ndarray] = None) -> np.ndarray:
-    """Fresh bf16 rows for a deterministic re-draw (attempt number as sub-stream)."""
+def redraw_rows(seed: int, tensor_name: str, row: int, attempt: int, shape: tuple,
+                dist: str) -> np.ndarray:
+    """Fresh bf16 bits for one leading-axis row of a tensor (e.g. one token's
+    idx_q rows, shape [Hidx, d]), drawn like ``draw_tensor`` (with the
+    tensor's own channel vector for "channel") from the sub-stream
+    (seed, 100 + tensor, row, attempt): a re-draw is deterministic and does
+    not depend on which other rows were redrawn."""
     tid = {"q": _Q, "k": _K, "v": _V, "idx_q": _IQ, "idx_k": _IK}[tensor_name]
-    g = _rng(seed, 100 + tid, attempt)
-    x = g.standard_normal((n_rows, last), dtype=np.float32)
-    if dist_vector is not None:
-        x *= dist_vector
+    g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 100 + tid, row, attempt])))
+    last = shape[-1]
+    x = g.standard_normal(shape, dtype=np.float32)
+    if dist == "channel":
+        x *= _channel_vector(seed, tid, last)
     return to_bf16_bits(x)
+
+
+def idx_q_redraw(w: "GQAWorkload"):
+    """The re-draw of one token's idx_q rows for a workload: a callable
+    (token, attempt) -> bf16 bits [Hidx, d_idx]."""
+    shape = w.idx_q.shape[1:]
+    return lambda t, attempt: redraw_rows(w.seed, "idx_q", t, attempt, shape, w.cfg.dist)
 
 
 @dataclass
@@ -161,6 +173,7 @@ class GQAWorkload:
     sink: np.ndarray            # fp32 [Hq]
     scales: Dict[str, float] = field(default_factory=dict)   # q, k, v, idx_q, idx_k
     sm_scale: float = 0.0
+    seed: int = 0
 
     @property
     def T(self) -> int:
@@ -217,7 +230,7 @@ def make_gqa(cfg: GQAConfig, seed: Optional[int] = None, T_override: Optional[in
         scales["k"] = float(np.float32(g.uniform(0.25, 4.0)))
         scales["v"] = float(np.float32(g.uniform(0.25, 4.0)))
     return GQAWorkload(cfg, seq_lens, cu_q, page_table, num_pages, q, idx_q, k_pool, v_pool,
-                       idx_k_pool, sink, scales, 1.0 / math.sqrt(cfg.D))
+                       idx_k_pool, sink, scales, 1.0 / math.sqrt(cfg.D), seed)
 
 
 @dataclass

@@ -111,6 +111,20 @@ msa_status msa_profile_last_ms(float* ms);
 msa_status msa_check_errors(msa_stream_t stream);
 
 /*
+ * Debug switch (tests of the failure path; off by default, per device).
+ * Every wait inside the library's kernels is bounded: when it runs out, the
+ * kernel records MSA_ERR_TIMEOUT in the device error word, every role of the
+ * block stops waiting, the block drains the copies and tensor-core
+ * operations it already issued (waiting at most 2 s for each), frees its
+ * tensor memory and returns. With on != 0, every wait that is not complete
+ * at its first test gives up at once, so a test can drive that path without
+ * anything hanging; the outputs of such calls are meaningless and the next
+ * msa_check_errors returns MSA_ERR_TIMEOUT. Synchronous (copies one word to
+ * the current device); call it outside graph capture.
+ */
+msa_status msa_debug_force_timeouts(int on);
+
+/*
  * Step (a): out[r, c] = e4m3_rn_satfinite( fp32(x[r, c]) * s_inv ),
  * s_inv = 1.0f / *scale computed once in fp32 on the host, or 1 when scale
  * is NULL. [25460] key source excerpt (fp8_quantize: widen, multiply by

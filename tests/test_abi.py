@@ -173,3 +173,19 @@ def test_header_is_plain_c99():
                         "-I", os.path.join(ROOT, "include"), "-fsyntax-only", "-x", "c", "-"],
                        input=src, capture_output=True, text=True)
     assert r.returncode == 0, r.stderr
+
+
+def test_noalloc_reports_argument_errors_before_its_scratch_limit(lib):
+    # sizes whose scratch would exceed the fixed array, but whose arguments are
+    # invalid or unsupported: the argument error is what comes back
+    p = ctypes.c_void_p(256)
+    T = 1 << 20
+    assert lib.msa_index_topk_noalloc(p, p, p, p, p, 1, T, T, 32, 128, 16, 64, 64, p, None) == 2
+    assert lib.msa_index_topk_noalloc(p, p, p, p, p, 1, T, T, 4, 96, 16, 64, 64, p, None) == 2
+    assert lib.msa_index_topk_noalloc(p, p, p, p, p, 1, T, T, 4, 128, 16, 64, 4096, p, None) == 2
+    assert lib.msa_index_topk_noalloc(p, p, p, p, p, 1, T, 0, 4, 128, 16, 64, 64, p, None) == 1
+    assert lib.msa_index_topk_noalloc(p, p, p, p, p, 0, T, T, 4, 128, 16, 64, 64, p, None) == 1
+    # the same unsupported sizes through the workspace entry point
+    assert lib.msa_index_topk(p, p, p, p, p, 1, T, T, 32, 128, 16, 64, 64, p, p, 1 << 40, None) == 2
+    # valid sizes over the scratch limit: the limit is reported
+    assert lib.msa_index_topk_noalloc(p, p, p, p, p, 1, T, T, 4, 128, 16, 64, 64, p, None) == 5

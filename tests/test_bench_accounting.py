@@ -78,13 +78,21 @@ def test_decode_bytes_read_each_union_block_once():
     assert total == idx_bytes + kv_bytes + small
 
 
-def test_committed_traffic_is_used_only_for_the_matching_source(monkeypatch):
-    summaries = ("attn_prefill_kernel_prefill32k_traffic.md", "attn_decode_kernel_decode_traffic.md")
-    for summary in summaries:
-        got = bench.traffic_for("attn.cu", summary)
-        assert got is not None and got > 0, summary      # the summary matches the current source
+def test_committed_traffic_is_used_only_for_the_matching_source(monkeypatch, tmp_path):
+    # a summary recording the hash of the kernel source it was taken on
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "k.md").write_text(
+        "# a kernel\n- source_hash: `00aa11bb22cc33dd`\n- dram_bytes_per_launch: 1234.5\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "src_hash", lambda *names: "00aa11bb22cc33dd")
+    assert bench.traffic_for("attn.cu", "k.md") == 1234.5
     assert bench.traffic_for("attn.cu", "missing.md") is None
-    # any change to the kernel source changes its hash: the figures are then not used
+    # any change to the kernel source changes its hash: the figure is then not used
     monkeypatch.setattr(bench, "src_hash", lambda *names: "0123456789abcdef")
-    for summary in summaries:
-        assert bench.traffic_for("attn.cu", summary) is None
+    assert bench.traffic_for("attn.cu", "k.md") is None
+
+
+def test_src_hash_follows_the_source_bytes():
+    h = bench.src_hash("attn.cu", "common.cuh")
+    assert len(h) == 16 and h == bench.src_hash("attn.cu", "common.cuh")
+    assert h != bench.src_hash("mla.cu", "common.cuh")

@@ -36,7 +36,7 @@ def fake(monkeypatch):
     lib = _FakeLib()
     monkeypatch.setattr(bd, "_LIB", lib)
     monkeypatch.setattr(bd, "_on_device", lambda t: True)
-    monkeypatch.setattr(bd, "_stream", lambda s: None)
+    monkeypatch.setattr(bd, "_stream", lambda s, d=None: None)
     return lib
 
 
@@ -198,3 +198,22 @@ def test_host_tensors_are_refused_by_the_real_library():
         with pytest.raises(bd.MsaError) as e:
             c()
         assert e.value.status == 1
+
+
+def test_tensors_on_two_devices_are_refused(fake):
+    # the library launches on one device: a call mixing devices would hand it
+    # another device's pointers, so the binding refuses it before the call
+    pt, sl, cu = _batch()
+    iq = torch.zeros((10, 4, 128), dtype=torch.uint8, device="meta")
+    ik = _u8(7, 128, 128)
+    n = len(fake.calls)
+    with pytest.raises(bd.MsaError, match="one device"):
+        bd.index_topk(iq, ik, pt, sl, cu, 16, 10)
+    with pytest.raises(bd.MsaError, match="one device"):
+        bd.index_topk_noalloc(iq, ik, pt, sl, cu, 16, 10)
+    q = torch.zeros((12, 16, 128), dtype=torch.uint8, device="meta")
+    kc = _u8(9, 2, 128, 128)
+    ids = torch.zeros((4, 12, 8), dtype=torch.int32)
+    with pytest.raises(bd.MsaError, match="one device"):
+        bd.sparse_attn_fwd(q, kc, kc.clone(), pt, sl, cu, ids, None, 0.1, None, None, None, 12)
+    assert len(fake.calls) == n

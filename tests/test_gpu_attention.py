@@ -10,7 +10,7 @@ import pytest
 
 from fp8_block_sparse_gb300 import workloads as wl
 from oracle import quant as oq, attention as oa
-from gpu_helpers import dev
+from gpu_helpers import dev, sample_tokens, sample_extremes
 
 pytestmark = pytest.mark.gpu
 
@@ -110,8 +110,7 @@ def test_prefill8k_sampled(msa):
 def test_prefill32k_sampled(msa):
     w = wl.make_gqa(wl.CONFIGS["prefill32k"])
     ids = wl.random_topk(2, w.seq_lens, w.cu_q, 4, 64)
-    tok = np.sort(np.random.default_rng(1).choice(w.T, size=48, replace=False))
-    run_attention(msa, w, np.ascontiguousarray(ids), tokens=np.concatenate([tok, [w.T - 1]]))
+    run_attention(msa, w, np.ascontiguousarray(ids), tokens=sample_tokens(w.T, 256, 1))
 
 
 def test_decode_small_contexts(msa):
@@ -142,7 +141,7 @@ def test_decode_config_sampled(msa):
                                      dev(w.cu_q), dev(ids), dev(w.sink), w.sm_scale, w.scales["q"],
                                      w.scales["k"], w.scales["v"], 1)
     msa.check_errors()
-    seqs = np.sort(np.random.default_rng(5).choice(w.cfg.B, size=8, replace=False))
+    seqs = sample_extremes(w.seq_lens, 32, 5)
     pages = np.unique(w.page_table[seqs][w.page_table[seqs] >= 0])
     k_ref = np.zeros((w.num_pages,) + w.k_pool.shape[1:], np.uint8)
     v_ref = np.zeros_like(k_ref)

@@ -10,7 +10,7 @@ import torch
 
 from fp8_block_sparse_gb300 import workloads as wl
 from oracle import quant as oq, mla as om
-from gpu_helpers import dev, dev_bf16
+from gpu_helpers import dev, dev_bf16, sample_extremes
 
 pytestmark = pytest.mark.gpu
 
@@ -68,7 +68,7 @@ def test_mla_config_sampled(msa):
     o, ml, lse = msa.sparse_mla_fwd(q8, dev(kv8), dev(w.indices), dev(w.topk_length), dev(w.sink),
                                     w.sm_scale, w.scales["q"], w.scales["kv"])
     msa.check_errors()
-    tok = np.sort(np.random.default_rng(0).choice(w.q.shape[0], size=6, replace=False))
+    tok = sample_extremes(w.topk_length, 64, 0)        # incl. the shortest and longest lists
     q8_ref = np.zeros((w.q.shape[0],) + w.q.shape[1:], np.uint8)
     q8_ref[tok] = oq.quantize(w.q[tok], w.scales["q"])
     assert np.array_equal(q8_ref[tok], q8.cpu().numpy()[tok])

@@ -19,6 +19,7 @@ import test_oracle_e4m3 as e4m3_pins
 import test_oracle_index_topk as index_pins
 import test_oracle_kv_store as kv_pins
 import test_oracle_mla as mla_pins
+import test_oracle_no_tie as no_tie_pins
 import test_oracle_quant as quant_pins
 import test_oracle_rope_quant as rope_pins
 
@@ -91,6 +92,16 @@ ROPE_MUTATIONS = [
 ]
 
 
+NO_TIE_MUTATIONS = [
+    ("return 2.0 * D * 2.0 ** -23 * s.max(axis=0)", "return D * 2.0 ** -23 * s.max(axis=0)"),
+    ("near = ~(gaps > bounds)", "near = gaps < bounds"),
+    ("keys = idx_k_codes[page_table[seq[t], :own]]", "keys = idx_k_codes[page_table[seq[t], 1:own]]"),
+    ("if int((fresh & np.uint16(0x7FFF)).max()) <= amax_bits:", "if True:"),
+    ("pending, _, _ = near_tie_tokens(codes, idx_k_codes, page_table, seq_lens, cu_q, topk,\n"
+     "                                        pending)", "pending = []"),
+]
+
+
 def _mutant(module: str, old: str, new: str) -> types.ModuleType:
     path = os.path.join(ORACLE_DIR, module + ".py")
     src = open(path).read()
@@ -144,6 +155,7 @@ def test_unmutated_oracles_pass_their_pins():
     assert not _pins_fail(mla_pins, "sparse_mla", same("mla").sparse_mla)
     assert not _pins_fail(kv_pins, "okv", same("kv_store"))
     assert not _pins_fail(rope_pins, "orq", same("rope_quant"))
+    assert not _pins_fail(no_tie_pins, "nt", same("no_tie"))
 
 
 @pytest.mark.parametrize("old,new", E4M3_MUTATIONS)
@@ -181,3 +193,8 @@ def test_kv_store_pins_catch(old, new):
 @pytest.mark.parametrize("old,new", ROPE_MUTATIONS)
 def test_rope_quant_pins_catch(old, new):
     assert _pins_fail(rope_pins, "orq", _mutant("rope_quant", old, new))
+
+
+@pytest.mark.parametrize("old,new", NO_TIE_MUTATIONS)
+def test_no_tie_pins_catch(old, new):
+    assert _pins_fail(no_tie_pins, "nt", _mutant("no_tie", old, new))
