@@ -22,8 +22,8 @@ float64 result can be predicted on the CPU:
 
 Where the kernels' design fixes it: the prefill kernel keeps P in f16 and
 moves the reference to the block maximum (limit 8, head 0); the decode kernel
-splits P into three e4m3 terms and moves the reference to 4 below the
-maximum (limit 8, head 4); the sparse-MLA kernel walks each query's index
+splits P into two e4m3 terms and moves the reference to 4 below the maximum
+(limit 8, head 4); the sparse-MLA kernel walks each query's index
 list in 64-entry chunks with f16 P (limit 8, head 0). MUFU's approximation
 error and the MMA's exact accumulation order are not modelled (both well
 below the roundings above).
@@ -47,7 +47,7 @@ LOG2E = 1.4426950408889634
 LN2 = 0.6931471805599453
 
 PREFILL = {"p_format": "f16", "limit": 8.0, "head": 0.0}
-DECODE = {"p_format": "e4m3x3", "limit": 8.0, "head": 4.0}
+DECODE = {"p_format": "e4m3x2", "limit": 8.0, "head": 4.0}
 
 
 def bf16_round(x: np.ndarray) -> np.ndarray:

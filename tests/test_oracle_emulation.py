@@ -4,7 +4,7 @@ With P kept in fp32 and no output rounding, the emulation's blockwise lazy
 softmax is algebraically the float64 oracle, so the two agree to fp32
 rounding: that pins the emulation. The other cases predict what each
 precision choice of the kernels costs against the float64 oracle: the
-designs built (f16 P in prefill, three e4m3 terms in decode) sit inside the
+designs built (f16 P in prefill, two e4m3 terms in decode) sit inside the
 parity bars, and a single e4m3 P term does not (which is why neither kernel
 uses it)."""
 
@@ -72,7 +72,7 @@ def test_prefill_design_f16_p_is_inside_the_bars(tiny):
     assert err <= BAR_ABS and rel <= BAR_REL and lerr <= BAR_LSE
 
 
-def test_decode_design_three_e4m3_terms_is_inside_the_bars(decode):
+def test_decode_design_two_e4m3_terms_is_inside_the_bars(decode):
     err, rel, lerr, _ = _errors(decode, **em.DECODE)
     assert err <= BAR_ABS and rel <= BAR_REL and lerr <= BAR_LSE
 
