@@ -3,7 +3,7 @@
 
 One step = the whole hot path over one batch of the 32k prefill workload
 (1 sequence x 32768 tokens, 16 q / 2 kv / 4 index heads, head_dim 128, top-k
-64 blocks of 128 tokens): quantise Q and idx_q, index scores + ascending
+64 blocks of 128 tokens): quantise Q and idx_q (one launch), index scores + ascending
 top-k, sparse attention with sink. The metric is prefill tokens/s; the same
 line reports the attention kernel's algorithmic TFLOP/s against the FP8
 tensor peak, the paged-decode workload's HBM GB/s (eager and as one CUDA
@@ -57,6 +57,9 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU oracle sample budget")
     p.add_argument("--no-e2e", action="store_true", help="skip the end-to-end measurement")
     p.add_argument("--no-mla", action="store_true", help="skip the sparse-MLA measurement")
+    p.add_argument("--only", choices=["prefill", "decode", "mla"], default=None,
+                   help="run only this part of the path, warm-up + steps times, untimed, and "
+                        "print no result line (for profiler captures)")
     p.add_argument("--workload", default=WORKLOAD, choices=["prefill32k", "prefill8k", "tiny"],
                    help="prefill workload of the step (the benchmark line uses prefill32k)")
     return p.parse_args()
@@ -192,15 +195,15 @@ def gqa_setup(msa, wl, name, dev, pinned=False):
     return st
 
 
-LAUNCHES_PREFILL = 2 + 3 + 3     # quant x2; index: plan, score, select; attn: plan, V^T, attention
+LAUNCHES_PREFILL = 1 + 3 + 3     # quant (Q and idx_q, one launch); index: plan, score, select; attn: plan, V^T, attention
 LAUNCHES_DECODE = 2 + 2 + 2      # quant x2; index: score, select; attn: decode, combine
 
 
 def run_path(msa, st, q_in=None, iq_in=None):
     w = st["w"]
     cfg = w.cfg
-    msa.quant_fp8(st["q"] if q_in is None else q_in, w.scales["q"], out=st["q8"])
-    msa.quant_fp8(st["iq"] if iq_in is None else iq_in, w.scales["idx_q"], out=st["iq8"])
+    msa.quant_fp8_multi([(st["q"] if q_in is None else q_in, w.scales["q"], st["q8"]),
+                         (st["iq"] if iq_in is None else iq_in, w.scales["idx_q"], st["iq8"])])
     msa.index_topk(st["iq8"], st["ik8"], st["pt"], st["sl"], st["cu"], cfg.topk, w.max_q_len,
                    out=st["ids"], workspace=st["ws_idx"])
     msa.sparse_attn_fwd(st["q8"], st["k8"], st["v8"], st["pt"], st["sl"], st["cu"], st["ids"], st["sink"],
@@ -284,8 +287,9 @@ def decode_bytes(st):
     return idx_bytes + kv_bytes + small, kv_bytes, union
 
 
-def mla_measure(msa, wl, dev, steps, flush, pk):
-    """Sparse-MLA prefill workload: quantise Q + MLA kernel per step."""
+def mla_measure(msa, wl, dev, steps, flush, pk, only=None):
+    """Sparse-MLA prefill workload: quantise Q + MLA kernel per step (with
+    `only` = n: just run the step n times, untimed)."""
     import numpy as np
     import torch
     w = wl.make_mla(wl.CONFIGS["mla"])
@@ -305,6 +309,12 @@ def mla_measure(msa, wl, dev, steps, flush, pk):
         msa.sparse_mla_fwd(q8, kv8, idx, tl, sink, w.sm_scale, w.scales["q"], w.scales["kv"],
                            out=o, max_logits=ml, lse=ls)
 
+    if only is not None:
+        for _ in range(only):
+            step()
+        torch.cuda.synchronize()
+        msa.check_errors()
+        return None
     for _ in range(3):
         step()
     torch.cuda.synchronize()
@@ -531,6 +541,19 @@ def native_arm(args):
             dist.barrier()
         torch.cuda.synchronize()
 
+    if args.only is not None:
+        # one part of the path, untimed, for profiler captures
+        n = args.warmup + args.steps
+        if args.only == "mla":
+            mla_measure(msa, wl, dev, 0, None, pk, only=n)
+        else:
+            part = gqa_setup(msa, wl, args.workload if args.only == "prefill" else "decode", dev)
+            for _ in range(n):
+                run_path(msa, part)
+            torch.cuda.synchronize()
+            msa.check_errors()
+        return 0
+
     st = gqa_setup(msa, wl, args.workload, dev, pinned=True)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     msa.profile_enable(True)
@@ -556,8 +579,8 @@ def native_arm(args):
         ev[k][0].record(s)
         c = cuts[k]
         c[0].record(s)
-        msa.quant_fp8(st["q"], st["w"].scales["q"], out=st["q8"])
-        msa.quant_fp8(st["iq"], st["w"].scales["idx_q"], out=st["iq8"])
+        msa.quant_fp8_multi([(st["q"], st["w"].scales["q"], st["q8"]),
+                             (st["iq"], st["w"].scales["idx_q"], st["iq8"])])
         c[1].record(s)
         w = st["w"]
         msa.index_topk(st["iq8"], st["ik8"], st["pt"], st["sl"], st["cu"], w.cfg.topk, w.max_q_len,

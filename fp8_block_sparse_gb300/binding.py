@@ -48,6 +48,7 @@ _SIGNATURES = {
     "msa_debug_force_timeouts": ([_I], _I),
     "msa_profile_last_ms": ([_FP], _I),
     "msa_quant_fp8": ([_P, _I, _I64, _I64, _I64, _P, _I, _I64, _FP, _P], _I),
+    "msa_quant_fp8_multi": ([_P, _I, _I, _I, _P], _I),
     "msa_kv_store_fp8": ([_P, _P, _P, _I, _I64, _I64, _I64, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I,
                           _FP, _FP, _FP, _P, _P, _P, _P], _I),
     "msa_rope_quant_fp8": ([_P, _P, _I, _I64, _I, _I, _I, _I64, _I64, _I64, _I64, _P, _I, _P, _I,
@@ -203,6 +204,62 @@ def quant_fp8(x: torch.Tensor, scale: Optional[float] = None, out: Optional[torc
                                  rows, cols, x2.stride(0) if rows else cols, _ptr(o2), MSA_E4M3,
                                  o2.stride(0) if rows else cols, _scale(scale), _stream(stream, dev)))
     return out
+
+
+class _QuantTensor(ctypes.Structure):
+    """msa_quant_tensor of include/msa.h."""
+    _fields_ = [("x", ctypes.c_void_p), ("rows", ctypes.c_int64), ("cols", ctypes.c_int64),
+                ("x_row_stride", ctypes.c_int64), ("out", ctypes.c_void_p),
+                ("out_row_stride", ctypes.c_int64), ("scale", ctypes.POINTER(ctypes.c_float))]
+
+
+QUANT_MULTI_MAX = 8
+
+
+def quant_fp8_multi(items, stream=None):
+    """Several quantisations in one launch (step a for Q and idx_q together).
+
+    items: sequence of (x, scale) or (x, scale, out) with x bf16 / fp16 (one
+    dtype for all) and a contiguous last dimension; returns the e4m3 outputs,
+    each byte-identical to quant_fp8(x, scale)."""
+    lib = load()
+    if not 1 <= len(items) <= QUANT_MULTI_MAX:
+        raise MsaError(1, f"need 1..{QUANT_MULTI_MAX} tensors, got {len(items)}")
+    dt = items[0][0].dtype
+    if dt not in (torch.bfloat16, torch.float16):
+        raise MsaError(1, f"x must be bf16 or fp16, got {dt}")
+    descs = (_QuantTensor * len(items))()
+    keep, outs, tensors = [], [], []
+    for i, it in enumerate(items):
+        x, scale = it[0], it[1]
+        out = it[2] if len(it) > 2 else None
+        if x.dtype != dt:
+            raise MsaError(1, "all tensors must share one dtype")
+        if not _on_device(x):
+            raise MsaError(1, "x must be a CUDA tensor")
+        if x.stride(-1) != 1:
+            raise MsaError(1, "x must have a contiguous last dimension")
+        cols = x.shape[-1]
+        rows = x.numel() // cols if cols else 0
+        x2 = x.reshape(rows, cols) if x.dim() != 2 else x
+        if out is None:
+            out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+        _dev(out, "out", torch.uint8)
+        if out.numel() != x.numel():
+            raise MsaError(1, f"out must hold {x.numel()} elements, got {out.numel()}")
+        o2 = out.view(rows, cols)
+        sc = _scale(scale)
+        keep.append((x2, o2, sc))
+        descs[i] = _QuantTensor(x2.data_ptr(), rows, cols, x2.stride(0) if rows else cols,
+                                o2.data_ptr(), o2.stride(0) if rows else cols, sc)
+        outs.append(out)
+        tensors += [x, out]
+    dev = _device(*tensors)
+    with _on(dev):
+        _check(lib.msa_quant_fp8_multi(ctypes.cast(descs, ctypes.c_void_p), len(items),
+                                       MSA_BF16 if dt == torch.bfloat16 else MSA_FP16, MSA_E4M3,
+                                       _stream(stream, dev)))
+    return outs
 
 
 def _token_rows(x: Optional[torch.Tensor], name: str, inner: int):

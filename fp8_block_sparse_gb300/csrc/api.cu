@@ -236,6 +236,55 @@ msa_status msa_quant_fp8(const void* x, msa_dtype x_dtype, int64_t rows, int64_t
   return MSA_OK;
 }
 
+msa_status msa_quant_fp8_multi(const msa_quant_tensor* tensors, int n, msa_dtype x_dtype,
+                               msa_dtype out_dtype, msa_stream_t stream) {
+  const char* fn = "msa_quant_fp8_multi";
+  if (out_dtype == MSA_E5M2)
+    return fail(MSA_ERR_UNSUPPORTED, std::string(fn) + ": e5m2 output is not supported (e4m3 only)");
+  if (out_dtype != MSA_E4M3) return fail(MSA_ERR_INVALID_ARG, std::string(fn) + ": out_dtype must be MSA_E4M3");
+  if (x_dtype != MSA_BF16 && x_dtype != MSA_FP16)
+    return fail(MSA_ERR_INVALID_ARG, std::string(fn) + ": x_dtype must be MSA_BF16 or MSA_FP16");
+  if (tensors == nullptr || n < 1 || n > MSA_QUANT_MULTI_MAX)
+    return fail(MSA_ERR_INVALID_ARG, std::string(fn) + ": need 1 <= n <= MSA_QUANT_MULTI_MAX tensors");
+  float s_inv[MSA_QUANT_MULTI_MAX];
+  for (int i = 0; i < n; ++i) {            // every entry is validated before any launch
+    const msa_quant_tensor& t = tensors[i];
+    const std::string at = std::string(fn) + ": tensor " + std::to_string(i);
+    if (t.rows < 0 || t.cols < 0) return fail(MSA_ERR_INVALID_ARG, at + ": negative size");
+    float sc = 1.0f;
+    if (!read_scale(t.scale, &sc, (at + ": scale").c_str())) return MSA_ERR_INVALID_ARG;
+    s_inv[i] = t.scale == nullptr ? 1.0f : 1.0f / sc;
+    if (t.rows == 0 || t.cols == 0) continue;
+    if (t.x == nullptr || t.out == nullptr) return fail(MSA_ERR_INVALID_ARG, at + ": null pointer");
+    if (t.x_row_stride < t.cols || t.out_row_stride < t.cols)
+      return fail(MSA_ERR_INVALID_ARG, at + ": row stride smaller than cols");
+    if (!aligned(t.x, 2)) return fail(MSA_ERR_INVALID_ARG, at + ": x not 2-byte aligned");
+  }
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  QuantMulti q{};
+  for (int i = 0; i < n; ++i) {
+    const msa_quant_tensor& t = tensors[i];
+    if (t.rows == 0 || t.cols == 0) continue;
+    if (!quant_multi_eligible(t.x, t.out, t.rows, t.cols, t.x_row_stride, t.out_row_stride)) continue;
+    q.x[q.n] = static_cast<const uint4*>(t.x);
+    q.out[q.n] = static_cast<uint4*>(t.out);
+    q.chunks[q.n] = uint64_t(t.rows * t.cols) / 16;
+    q.s_inv[q.n] = s_inv[i];
+    ++q.n;
+  }
+  cudaError_t e = launch_quant_multi(q, x_dtype == MSA_BF16, st);
+  if (e != cudaSuccess) return cuda_fail(e, fn);
+  for (int i = 0; i < n; ++i) {            // the rest, one launch each
+    const msa_quant_tensor& t = tensors[i];
+    if (t.rows == 0 || t.cols == 0) continue;
+    if (quant_multi_eligible(t.x, t.out, t.rows, t.cols, t.x_row_stride, t.out_row_stride)) continue;
+    e = launch_quant(t.x, x_dtype == MSA_BF16, t.rows, t.cols, t.x_row_stride,
+                     static_cast<uint8_t*>(t.out), t.out_row_stride, s_inv[i], st);
+    if (e != cudaSuccess) return cuda_fail(e, fn);
+  }
+  return MSA_OK;
+}
+
 msa_status msa_kv_store_fp8(const void* k, const void* v, const void* idx_k, msa_dtype in_dtype,
                             int64_t k_token_stride, int64_t v_token_stride,
                             int64_t idx_k_token_stride, const int32_t* page_table,

@@ -61,6 +61,8 @@ __global__ void __launch_bounds__(256)
 vt_convert_kernel(const uint8_t* __restrict__ v_cache, const int32_t* __restrict__ page_table,
                   const int32_t* __restrict__ seq_lens, int Hkv, int max_pages, int num_pages,
                   uint8_t* __restrict__ vt_img, unsigned* err) {
+  pdl_wait();      // the V cache and batch description may come from earlier kernels
+  pdl_trigger();
   const int blk = blockIdx.x, b = blockIdx.y, g = blockIdx.z;
   const int L = seq_lens[b];
   if (L <= blk * 128 || L > max_pages * 128) return;
@@ -112,6 +114,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     int Hidx, int toks, int topk_k, int max_pages, int num_pages,
                     uint16_t* __restrict__ out, float* __restrict__ max_logit,
                     float* __restrict__ lse, unsigned* err) {
+  pdl_wait();      // tiles, V images, queries and top-k come from earlier kernels
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   __shared__ uint64_t bar_q, bar_kf[kStages], bar_ke[kStages], bar_vf[kStages], bar_ve[kStages],
@@ -147,6 +150,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   }
   if (warp == 1) { tmem_alloc(&tmem_base_s, 512); tmem_relinquish(); }
   __syncthreads();
+  pdl_trigger();   // after this block's tensor-memory allocation
 
   // ---- softmax threads own rows: row = 128*X + 32*(warp%4) + lane
   const bool is_softmax = warp >= 4;
@@ -295,77 +299,148 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       // S_X(j) done (and with it PV_X(j-1): O is settled and P may be rewritten)
       if (!mbar_wait_warp(&bar_sf[X], j & 1, err, &abort_s)) break;   // uniform: tcgen05 ops follow
       tc_fence_after();
-      float x[128];
-      {
-        uint32_t v[128];
-        tmem_ld128(s_col, v);
-#pragma unroll
-        for (int e = 0; e < 128; ++e) x[e] = __uint_as_float(v[e]);
-      }
-      // row max of the raw scores over the valid columns (scale > 0 commutes)
-      float mr = -INFINITY;
-      if (ncol == 128) {
-        float a0 = x[0], a1 = x[1], a2 = x[2], a3 = x[3];
-#pragma unroll
-        for (int c = 4; c < 128; c += 8) {
-          a0 = fmax3(a0, x[c], x[c + 1]);
-          a1 = fmax3(a1, x[c + 2], x[c + 3]);
-          a2 = fmax3(a2, x[c + 4], x[c + 5]);
-          a3 = fmax3(a3, x[c + 6], x[c + 7]);
-        }
-        mr = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
-      } else if (ncol > 0) {
-#pragma unroll
-        for (int c = 0; c < 128; ++c) mr = (c < ncol) ? fmaxf(mr, x[c]) : mr;
-      }
-      const float mx = mr * qk_scale2;
-      m_true = fmaxf(m_true, mx);
-      const bool grow = mx > m + kRescale;                    // also when m == -inf
-      const bool need_rescale = grow && (m > -INFINITY);
-      if (__any_sync(0xffffffffu, need_rescale)) {
-        const float alpha = need_rescale ? exp2f(m - mx) : 1.0f;
-#pragma unroll
-        for (int c = 0; c < 128; c += 16) {
-          uint32_t v[16];
-          tmem_ld16(o_col + c, v);
-#pragma unroll
-          for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-          tmem_st16(o_col + c, v);
-        }
-        if (need_rescale) l *= alpha;
-      }
-      if (grow) m = mx;
-
-      // P = exp2(S * scale - m) as f16 pairs over the first 64 columns of S_X.
-      // Three explicit paths so the common full block carries no masking.
-      uint32_t w[64];
-      if (ncol == 128) {
+      const bool live = ncol == 128;
+      // Speculative path, taken when every lane's row uses the whole block or
+      // none of it and no row is at its first block (so m is finite): the
+      // exponentials use the current reference m while the block maximum is
+      // reduced alongside, and S is loaded and P stored in 32-key chunks so
+      // that loads, exponentials and stores overlap. Only when some row's
+      // maximum outgrows m by 2^8 is the block redone with the new reference.
+      if (!__any_sync(0xffffffffu, (ncol > 0 && ncol < 128) || (live && m == -INFINITY))) {
+        uint32_t xs[128];
+        uint32_t w[64];
         const uint64_t negm = pk2(-m, -m);
         uint64_t acc0 = pk2(0.f, 0.f), acc1 = acc0;
+        float mr = -INFINITY;
+        tmem_ld32_async(s_col, slice32(xs, 0));
+        tmem_wait_ld32(slice32(xs, 0));
 #pragma unroll
-        for (int c = 0; c < 128; c += 2) {
-          const float2 y = unpk2(ffma2(pk2(x[c], x[c + 1]), scale2, negm));
-          const float p0 = fast_exp2(y.x), p1 = fast_exp2(y.y);
-          if (c & 2) acc1 = fadd2(acc1, pk2(p0, p1)); else acc0 = fadd2(acc0, pk2(p0, p1));
-          w[c >> 1] = pack_f16x2(p0, p1);
-        }
-        const float2 a2 = unpk2(fadd2(acc0, acc1));
-        l += a2.x + a2.y;
-      } else if (ncol > 0) {
-        float sum = 0.f;
+        for (int c = 0; c < 4; ++c) {
+          if (c < 3) tmem_ld32_async(s_col + 32 * (c + 1), slice32(xs, c + 1));
+          float a0 = __uint_as_float(xs[32 * c]), a1 = __uint_as_float(xs[32 * c + 1]);
 #pragma unroll
-        for (int c = 0; c < 128; c += 2) {
-          const float p0 = c < ncol ? fast_exp2(fmaf(x[c], qk_scale2, -m)) : 0.f;
-          const float p1 = c + 1 < ncol ? fast_exp2(fmaf(x[c + 1], qk_scale2, -m)) : 0.f;
-          sum += p0 + p1;
-          w[c >> 1] = pack_f16x2(p0, p1);
+          for (int e = 2; e < 32; e += 4) {
+            a0 = fmax3(a0, __uint_as_float(xs[32 * c + e]), __uint_as_float(xs[32 * c + e + 1]));
+            a1 = fmax3(a1, __uint_as_float(xs[32 * c + e + 2]), __uint_as_float(xs[32 * c + e + 3]));
+          }
+          mr = fmax3(mr, a0, a1);
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float2 y = unpk2(ffma2(pk2(__uint_as_float(xs[32 * c + e]),
+                                             __uint_as_float(xs[32 * c + e + 1])), scale2, negm));
+            const float p0 = fast_exp2(y.x), p1 = fast_exp2(y.y);
+            if (e & 2) acc1 = fadd2(acc1, pk2(p0, p1)); else acc0 = fadd2(acc0, pk2(p0, p1));
+            w[16 * c + (e >> 1)] = live ? pack_f16x2(p0, p1) : 0u;
+          }
+          tmem_st16_async(s_col + 16 * c, slice16(w, c));
+          if (c < 3) tmem_wait_ld32(slice32(xs, c + 1));
         }
-        l += sum;
+        tmem_wait_st64(w);
+        const float mx = live ? mr * qk_scale2 : -INFINITY;
+        m_true = fmaxf(m_true, mx);
+        const bool grow = mx > m + kRescale;
+        if (__any_sync(0xffffffffu, grow)) {
+          // some row's maximum outgrew its reference: rescale O and l, redo P
+          const float alpha = grow ? exp2f(m - mx) : 1.0f;
+#pragma unroll
+          for (int c = 0; c < 128; c += 16) {
+            uint32_t v[16];
+            tmem_ld16(o_col + c, v);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+            tmem_st16(o_col + c, v);
+          }
+          if (grow) { l *= alpha; m = mx; }
+          const uint64_t negm2 = pk2(-m, -m);
+          acc0 = pk2(0.f, 0.f);
+          acc1 = acc0;
+#pragma unroll
+          for (int e = 0; e < 128; e += 2) {
+            const float2 y = unpk2(ffma2(pk2(__uint_as_float(xs[e]), __uint_as_float(xs[e + 1])),
+                                         scale2, negm2));
+            const float p0 = fast_exp2(y.x), p1 = fast_exp2(y.y);
+            if (e & 2) acc1 = fadd2(acc1, pk2(p0, p1)); else acc0 = fadd2(acc0, pk2(p0, p1));
+            w[e >> 1] = live ? pack_f16x2(p0, p1) : 0u;
+          }
+          tmem_st64(s_col, w);
+        }
+        if (live) {
+          const float2 a2 = unpk2(fadd2(acc0, acc1));
+          l += a2.x + a2.y;
+        }
       } else {
-#pragma unroll
-        for (int c = 0; c < 64; ++c) w[c] = 0u;
+        float x[128];
+        {
+          uint32_t v[128];
+          tmem_ld128(s_col, v);
+  #pragma unroll
+          for (int e = 0; e < 128; ++e) x[e] = __uint_as_float(v[e]);
+        }
+        // row max of the raw scores over the valid columns (scale > 0 commutes)
+        float mr = -INFINITY;
+        if (ncol == 128) {
+          float a0 = x[0], a1 = x[1], a2 = x[2], a3 = x[3];
+  #pragma unroll
+          for (int c = 4; c < 128; c += 8) {
+            a0 = fmax3(a0, x[c], x[c + 1]);
+            a1 = fmax3(a1, x[c + 2], x[c + 3]);
+            a2 = fmax3(a2, x[c + 4], x[c + 5]);
+            a3 = fmax3(a3, x[c + 6], x[c + 7]);
+          }
+          mr = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
+        } else if (ncol > 0) {
+  #pragma unroll
+          for (int c = 0; c < 128; ++c) mr = (c < ncol) ? fmaxf(mr, x[c]) : mr;
+        }
+        const float mx = mr * qk_scale2;
+        m_true = fmaxf(m_true, mx);
+        const bool grow = mx > m + kRescale;                    // also when m == -inf
+        const bool need_rescale = grow && (m > -INFINITY);
+        if (__any_sync(0xffffffffu, need_rescale)) {
+          const float alpha = need_rescale ? exp2f(m - mx) : 1.0f;
+  #pragma unroll
+          for (int c = 0; c < 128; c += 16) {
+            uint32_t v[16];
+            tmem_ld16(o_col + c, v);
+  #pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+            tmem_st16(o_col + c, v);
+          }
+          if (need_rescale) l *= alpha;
+        }
+        if (grow) m = mx;
+
+        // P = exp2(S * scale - m) as f16 pairs over the first 64 columns of S_X.
+        // Three explicit paths so the common full block carries no masking.
+        uint32_t w[64];
+        if (ncol == 128) {
+          const uint64_t negm = pk2(-m, -m);
+          uint64_t acc0 = pk2(0.f, 0.f), acc1 = acc0;
+  #pragma unroll
+          for (int c = 0; c < 128; c += 2) {
+            const float2 y = unpk2(ffma2(pk2(x[c], x[c + 1]), scale2, negm));
+            const float p0 = fast_exp2(y.x), p1 = fast_exp2(y.y);
+            if (c & 2) acc1 = fadd2(acc1, pk2(p0, p1)); else acc0 = fadd2(acc0, pk2(p0, p1));
+            w[c >> 1] = pack_f16x2(p0, p1);
+          }
+          const float2 a2 = unpk2(fadd2(acc0, acc1));
+          l += a2.x + a2.y;
+        } else if (ncol > 0) {
+          float sum = 0.f;
+  #pragma unroll
+          for (int c = 0; c < 128; c += 2) {
+            const float p0 = c < ncol ? fast_exp2(fmaf(x[c], qk_scale2, -m)) : 0.f;
+            const float p1 = c + 1 < ncol ? fast_exp2(fmaf(x[c + 1], qk_scale2, -m)) : 0.f;
+            sum += p0 + p1;
+            w[c >> 1] = pack_f16x2(p0, p1);
+          }
+          l += sum;
+        } else {
+  #pragma unroll
+          for (int c = 0; c < 64; ++c) w[c] = 0u;
+        }
+        tmem_st64(s_col, w);
       }
-      tmem_st64(s_col, w);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_pf[X]);
@@ -479,6 +554,7 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                    int Hkv, int Hidx, int topk_k, int max_pages, int num_pages, int max_chunks,
                    float* __restrict__ part_o, DecodePartial* __restrict__ part_s,
                    int* __restrict__ n_chunks_out, unsigned* err) {
+  pdl_wait();      // queries, caches and top-k may come from earlier kernels
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   __shared__ uint64_t bar_q, bar_kf[kDecKStages], bar_ke[kDecKStages], bar_vf[kDecVStages],
@@ -581,6 +657,7 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
   }
   if (warp == 1) { tmem_alloc(&tmem_base_s, 64); tmem_relinquish(); }
   __syncthreads();
+  pdl_trigger();   // after this block's tensor-memory allocation
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;          // S^T buffers at cols 0, 16; O^T at 32
 
@@ -829,6 +906,8 @@ decode_combine_kernel(const float* __restrict__ part_o, const DecodePartial* __r
                       float sink_scale2, float v_scale, int Hq, int Hkv, int max_chunks,
                       uint16_t* __restrict__ out, float* __restrict__ max_logit,
                       float* __restrict__ lse) {
+  pdl_wait();      // the chunk partials come from the decode kernel
+  pdl_trigger();
   const int t = blockIdx.x / Hkv, g = blockIdx.x % Hkv;
   const int G = Hq / Hkv;
   const size_t unit = size_t(t) * Hkv + g;
@@ -895,16 +974,14 @@ cudaError_t launch_decode(const AttnArgs& a, cudaStream_t stream, const char** w
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecodeSmem);
   if (e != cudaSuccess) return e;
   profile_mark(stream, 0);
-  kern<<<a.T * a.Hkv * mc, kDecThreads, kDecodeSmem, stream>>>(
-      tm_q, tm_k, tm_v, a.page_table, a.seq_lens, a.cu_q, a.topk, a.c_qk * kLog2e, a.B, a.T, a.Hq,
-      a.Hkv, a.Hidx, a.topk_k, a.max_pages, a.num_pages, mc, part_o, part_s, n_chunks, a.err);
+  e = launch_pdl(kern, a.T * a.Hkv * mc, kDecThreads, kDecodeSmem, stream, tm_q, tm_k, tm_v,
+                 a.page_table, a.seq_lens, a.cu_q, a.topk, a.c_qk * kLog2e, a.B, a.T, a.Hq, a.Hkv,
+                 a.Hidx, a.topk_k, a.max_pages, a.num_pages, mc, part_o, part_s, n_chunks, a.err);
   profile_mark(stream, 1);
-  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  decode_combine_kernel<<<a.T * a.Hkv, 256, 0, stream>>>(part_o, part_s, n_chunks, a.sink,
-                                                         a.c_sink * kLog2e, a.v_scale, a.Hq, a.Hkv,
-                                                         mc, a.out, a.max_logit, a.lse);
-  return cudaGetLastError();
+  return launch_pdl(decode_combine_kernel, a.T * a.Hkv, 256, 0, stream, part_o, part_s, n_chunks,
+                    a.sink, a.c_sink * kLog2e, a.v_scale, a.Hq, a.Hkv, mc, a.out, a.max_logit,
+                    a.lse);
 }
 
 }  // namespace
@@ -954,22 +1031,23 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, cudaStream_t stream, const cha
                            CU_TENSOR_MAP_SWIZZLE_128B, why))
       return cudaErrorInvalidValue;
   }
-  plan_tiles_kernel<<<1, 256, 0, stream>>>(a.seq_lens, a.cu_q, a.B, 2 * toks, a.max_pages,
-                                           max_tiles, tiles, n_tiles, a.err);
-  vt_convert_kernel<<<dim3(a.max_pages, a.B, a.Hkv), 256, 0, stream>>>(
-      a.v_cache, a.page_table, a.seq_lens, a.Hkv, a.max_pages, a.num_pages, ws, a.err);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(plan_tiles_kernel, 1, 256, 0, stream, a.seq_lens, a.cu_q, a.B, 2 * toks,
+                             a.max_pages, max_tiles, tiles, n_tiles, a.err);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(vt_convert_kernel, dim3(a.max_pages, a.B, a.Hkv), 256, 0, stream, a.v_cache,
+                 a.page_table, a.seq_lens, a.Hkv, a.max_pages, a.num_pages, ws, a.err);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(attn_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrefillSmem);
   if (e != cudaSuccess) return e;
   const int grid = ((a.T + 2 * toks - 1) / (2 * toks) + a.B) * a.Hkv;
   profile_mark(stream, 0);
-  attn_prefill_kernel<<<grid, kPrefillThreads, kPrefillSmem, stream>>>(
-      tm_q, tm_k, ws, a.page_table, tiles, n_tiles, a.topk, a.sink, a.c_qk * kLog2e,
-      a.c_sink * kLog2e, a.v_scale, a.T, a.Hq, a.Hkv, a.Hidx, toks, a.topk_k, a.max_pages,
-      a.num_pages, a.out, a.max_logit, a.lse, a.err);
+  e = launch_pdl(attn_prefill_kernel, grid, kPrefillThreads, kPrefillSmem, stream, tm_q, tm_k,
+                 static_cast<const uint8_t*>(ws), a.page_table, static_cast<const TileInfo*>(tiles),
+                 static_cast<const int*>(n_tiles), a.topk, a.sink, a.c_qk * kLog2e,
+                 a.c_sink * kLog2e, a.v_scale, a.T, a.Hq, a.Hkv, a.Hidx, toks, a.topk_k,
+                 a.max_pages, a.num_pages, a.out, a.max_logit, a.lse, a.err);
   profile_mark(stream, 1);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace msa

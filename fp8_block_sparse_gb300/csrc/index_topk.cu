@@ -61,6 +61,7 @@ index_score_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                            const TileInfo* __restrict__ tiles, const int* __restrict__ n_tiles_p,
                            int T, int Hidx, int toks, int max_pages, int num_pages,
                            int chunks_per_tile, float* __restrict__ scores, unsigned* err) {
+  pdl_wait();      // the tile list, queries and cache come from earlier kernels
   constexpr int SWZ = D;                    // 128-byte or 64-byte swizzle rows
   constexpr uint32_t kIdesc = idesc_f32(128, 128);
   using L = PrefillSmem<D>;
@@ -97,6 +98,7 @@ index_score_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
   }
   if (warp == 1) { tmem_alloc(&tmem_base_s, 256); tmem_relinquish(); }
   __syncthreads();
+  pdl_trigger();   // after this block's tensor-memory allocation
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
 
@@ -184,6 +186,7 @@ index_score_decode_kernel(const __grid_constant__ CUtensorMap tm_q,
                           const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ cu_q,
                           int B, int T, int Hidx, int max_pages, int num_pages,
                           int chunks_per_tok, float* __restrict__ scores, unsigned* err) {
+  pdl_wait();      // queries, cache and batch description may come from earlier kernels
   constexpr int SWZ = D;
   constexpr int kBufs = 4;
   constexpr uint32_t kIdesc = idesc_f32(128, 16);
@@ -222,6 +225,7 @@ index_score_decode_kernel(const __grid_constant__ CUtensorMap tm_q,
   }
   if (warp == 1) { tmem_alloc(&tmem_base_s, 64); tmem_relinquish(); }
   __syncthreads();
+  pdl_trigger();   // after this block's tensor-memory allocation
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
 
@@ -305,6 +309,8 @@ __global__ void __launch_bounds__(256)
 topk_select_kernel(const float* __restrict__ scores, const int32_t* __restrict__ seq_lens,
                    const int32_t* __restrict__ cu_q, int B, int T, int Hidx, int topk,
                    int max_pages, int32_t* __restrict__ out, unsigned* err) {
+  pdl_wait();      // the scores come from the scoring kernel
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (row >= (long long)Hidx * T) return;
@@ -429,33 +435,30 @@ cudaError_t launch_index_topk(const IndexArgs& a, cudaStream_t stream, const cha
     auto kern = D == 128 ? index_score_decode_kernel<128> : index_score_decode_kernel<64>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    kern<<<a.T * chunks, 192, smem, stream>>>(tm_q, tm_k, a.page_table, a.seq_lens, a.cu_q, a.B, a.T,
-                                              a.Hidx, a.max_pages, a.num_pages, chunks, scores, a.err);
+    e = launch_pdl(kern, a.T * chunks, 192, smem, stream, tm_q, tm_k, a.page_table, a.seq_lens,
+                   a.cu_q, a.B, a.T, a.Hidx, a.max_pages, a.num_pages, chunks, scores, a.err);
+    if (e != cudaSuccess) return e;
   } else {
-    plan_tiles_kernel<<<1, 256, 0, stream>>>(a.seq_lens, a.cu_q, a.B, toks, a.max_pages, max_tiles,
-                                            tiles, n_tiles, a.err);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(plan_tiles_kernel, 1, 256, 0, stream, a.seq_lens, a.cu_q, a.B, toks,
+                               a.max_pages, max_tiles, tiles, n_tiles, a.err);
     if (e != cudaSuccess) return e;
     const int smem = D == 128 ? PrefillSmem<128>::kBytes : PrefillSmem<64>::kBytes;
     auto kern = D == 128 ? index_score_prefill_kernel<128> : index_score_prefill_kernel<64>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int n_tiles_max = (a.T + toks - 1) / toks + a.B;
-    kern<<<n_tiles_max * chunks, 192, smem, stream>>>(tm_q, tm_k, a.page_table, tiles, n_tiles, a.T,
-                                                      a.Hidx, toks, a.max_pages, a.num_pages, chunks,
-                                                      scores, a.err);
+    e = launch_pdl(kern, n_tiles_max * chunks, 192, smem, stream, tm_q, tm_k, a.page_table, tiles,
+                   n_tiles, a.T, a.Hidx, toks, a.max_pages, a.num_pages, chunks, scores, a.err);
+    if (e != cudaSuccess) return e;
   }
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
   const long long rows = (long long)a.Hidx * a.T;
   const int grid = int((rows + 7) / 8);
   if (a.max_pages <= 256)
-    topk_select_kernel<8><<<grid, 256, 0, stream>>>(scores, a.seq_lens, a.cu_q, a.B, a.T, a.Hidx, a.topk, a.max_pages, a.topk_indices, a.err);
+    return launch_pdl(topk_select_kernel<8>, grid, 256, 0, stream, scores, a.seq_lens, a.cu_q, a.B, a.T, a.Hidx, a.topk, a.max_pages, a.topk_indices, a.err);
   else if (a.max_pages <= 512)
-    topk_select_kernel<16><<<grid, 256, 0, stream>>>(scores, a.seq_lens, a.cu_q, a.B, a.T, a.Hidx, a.topk, a.max_pages, a.topk_indices, a.err);
+    return launch_pdl(topk_select_kernel<16>, grid, 256, 0, stream, scores, a.seq_lens, a.cu_q, a.B, a.T, a.Hidx, a.topk, a.max_pages, a.topk_indices, a.err);
   else
-    topk_select_kernel<64><<<grid, 256, 0, stream>>>(scores, a.seq_lens, a.cu_q, a.B, a.T, a.Hidx, a.topk, a.max_pages, a.topk_indices, a.err);
-  return cudaGetLastError();
+    return launch_pdl(topk_select_kernel<64>, grid, 256, 0, stream, scores, a.seq_lens, a.cu_q, a.B, a.T, a.Hidx, a.topk, a.max_pages, a.topk_indices, a.err);
 }
 
 }  // namespace msa

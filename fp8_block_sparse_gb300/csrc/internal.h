@@ -8,6 +8,7 @@
 #include <stdint.h>
 
 #include <string>
+#include <utility>
 
 #include "msa.h"
 
@@ -39,6 +40,29 @@ bool encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, int rank, co
 
 int num_sms();
 
+// Launches a kernel with programmatic stream serialisation (programmatic
+// dependent launch): its blocks may be scheduled while the previous kernel in
+// the stream is still finishing, and wait in griddepcontrol.wait (pdl_wait)
+// for that kernel's completion before touching global memory. Every kernel of
+// the library begins with that wait, in every block, so a kernel never
+// completes before the one it follows and the chain stays ordered; outside a
+// chain of such kernels the attribute changes nothing.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // Instrumentation: records the start (which = 0) or stop (which = 1) event
 // around a main attention kernel when profiling is enabled; no-op otherwise.
 void profile_mark(cudaStream_t stream, int which);
@@ -46,6 +70,21 @@ void profile_mark(cudaStream_t stream, int which);
 // Step (a).
 cudaError_t launch_quant(const void* x, bool bf16, int64_t rows, int64_t cols, int64_t x_stride,
                          uint8_t* out, int64_t out_stride, float s_inv, cudaStream_t stream);
+
+// Step (a) over several contiguous tensors in one launch (blocks are dealt
+// to the tensors in proportion to their sizes).
+struct QuantMulti {
+  int n;
+  const uint4* x[MSA_QUANT_MULTI_MAX];
+  uint4* out[MSA_QUANT_MULTI_MAX];
+  uint64_t chunks[MSA_QUANT_MULTI_MAX];    // 16-element chunks of each tensor
+  float s_inv[MSA_QUANT_MULTI_MAX];
+  int block0[MSA_QUANT_MULTI_MAX + 1];     // first block of each tensor; block0[n] = grid
+};
+cudaError_t launch_quant_multi(QuantMulti& q, bool bf16, cudaStream_t stream);
+// Whether msa_quant_fp8_multi can take this tensor into its single launch.
+bool quant_multi_eligible(const void* x, const void* out, int64_t rows, int64_t cols,
+                          int64_t x_stride, int64_t out_stride);
 
 // The quantised KV-cache store (before the path). Token strides in elements.
 struct KvStoreArgs {

@@ -12,25 +12,29 @@
 //
 // GB300 design. The 128 heads of one query share its index list, so they are
 // the M = 128 rows of every MMA. A CTA owns one query token and one half of
-// d_v: the full 128 x 512 fp32 O would take all 512 TMEM columns, leaving
-// none for S, so each half keeps a 256-column O and recomputes S (the QK^T
-// part is 53% of the flops; duplicating it costs 1.5x the MMA work of one CTA
-// per token, and the two halves run as separate CTAs on different SMs).
-// Per 64-key chunk of the index list:
+// d_v (a 128 x 512 fp32 O alone would fill all 512 TMEM columns), so both
+// halves compute S. TMEM: the 512 nope bytes of Q per head (columns 0-127,
+// four e4m3 per column: the A operand of QK^T, so the largest operand is not
+// read from shared memory once per chunk), two 64-column S buffers, and the
+// 256-column O half. Per 64-entry chunk of the index list:
 //   gather   four warps copy the 64 kv rows (576 B each; a whole warp per
 //            row, 16-byte cp.async, indices loaded one chunk ahead) into a
 //            K-major tile: four 128-byte swizzled regions plus one 64-byte
 //            swizzled region for the last 64 columns; invalid entries become
-//            zero rows (and are masked);
-//   S = Q K^T  tcgen05 e4m3, M=128, N=64, K=576 (18 MMAs), double-buffered TMEM;
-//   V        four more warps widen this CTA's 256 V columns of the tile to
-//            f16 in place of layout (rows = keys, 16-byte loads, two 16-byte
-//            stores each, no transpose) into a double-buffered image, while
-//            the gather warps fetch the next chunk; PV reads it as an MN-major
-//            operand;
-//   P        one thread per head row: online softmax with lazy rescale, P in
-//            f16 (e4m3 P costs ~2.5% relative error on flat rows);
-//   O += P V tcgen05 kind::f16, M=128, N=256, K=64, B (V) MN-major.
+//            zero rows (and are masked); four stages;
+//   S = Q K^T  tcgen05 e4m3, M=128, N=64: 16 MMAs with A = Q's nope part in
+//            TMEM, 2 with A = its rope part in shared memory;
+//   P        one thread per head row: online softmax with a lazy reference 4
+//            below the running maximum (moved only when a chunk's maximum
+//            exceeds it by 2^8, so P <= 2^8 < 448); P is split into two e4m3
+//            terms (P rounded, then its rounded remainder), written over the
+//            first 32 columns of the chunk's own S buffer;
+//   O += P V tcgen05 e4m3, M=128, N=256, K=64 per term: A = the P terms in
+//            TMEM, B = this CTA's 256 V columns read straight out of the
+//            gathered tile as an MN-major operand (no conversion pass).
+// Two e4m3 terms carry P to about 2^-8 of its value: emulated on the CPU over
+// full-size queries they cost no more than f16 P (the bf16 rounding of O
+// dominates both), while a single e4m3 term costs ~2% relative error.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -42,24 +46,24 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescale = 8.0f;
-constexpr int kDqk = 576, kDv = 512, kChunkKeys = 64;
+constexpr float kLimit = 8.0f;    // log2 of the largest P before the reference moves
+constexpr float kHead = 4.0f;     // log2 of P at the key that set the reference
+constexpr int kDqk = 576, kDv = 512, kChunkKeys = 64, kStagesM = 4;
 
 // shared memory (byte offsets from a 1024-aligned base)
 constexpr int kQOff = 0;            // 128 x 576 e4m3: 4 x 16 KB (SW128) + 8 KB (SW64)
 constexpr int kQTail = 65536;
-constexpr int kKOff = 73728;        // 2 stages x 36 KB: 4 x 8 KB (SW128) + 4 KB (SW64)
+constexpr int kKOff = 73728;        // kStagesM stages x 36 KB: 4 x 8 KB (SW128) + 4 KB (SW64)
 constexpr int kKStage = 36864;
 constexpr int kKTail = 32768;       // offset of the SW64 region inside a stage
-constexpr int kVTOff = 147456;      // 2 x (64 keys x 256 f16 V: 4 blocks of 64 columns, 8 KB each, SW128)
-constexpr int kMlaSmem = 212992 + 1024;
-// TMEM columns: S_s at 64*s, P_s (f16 pairs) at 128 + 32*s, O at 256
-constexpr uint32_t kTP = 128, kTO = 256;
+constexpr int kMlaSmem = kKOff + kStagesM * kKStage + 1024;
+// TMEM columns: Q nope at 0, S_b at 128 + 64*b (P terms over its first 32), O at 256
+constexpr uint32_t kTS = 128, kTO = 256;
 
 constexpr uint32_t kIdescQK = idesc_f32(128, 64);
 constexpr uint32_t kIdescPV = idesc_f32(128, 256) | (1u << 16);   // B MN-major
 
-constexpr int kMlaThreads = 416;   // MMA, 4 gather, 4 softmax, 4 widening warps
+constexpr int kMlaThreads = 288;   // MMA, 4 gather, 4 softmax warps
 
 __global__ void __launch_bounds__(kMlaThreads, 1)
 mla_prefill_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_constant__ CUtensorMap tm_q64,
@@ -68,10 +72,11 @@ mla_prefill_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_con
                    float qk_scale2, float sink_scale2, float v_scale, int T, int S_kv, int topk,
                    uint16_t* __restrict__ out, float* __restrict__ max_logits,
                    float* __restrict__ lse, unsigned* err) {
+  pdl_wait();      // queries, latent cache and indices may come from earlier kernels
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  __shared__ uint64_t bar_q, bar_kf[2], bar_ke[2], bar_sf[2], bar_se[2], bar_pf[2], bar_pe[2],
-      bar_vtf[2], bar_vte[2], bar_pv, bar_done, bar_drain;
+  __shared__ uint64_t bar_q, bar_qt, bar_kf[kStagesM], bar_ke[kStagesM], bar_sf[2], bar_pf[2],
+      bar_pv, bar_done, bar_drain;
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_s;
 
@@ -85,18 +90,17 @@ mla_prefill_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_con
   if (tid == 0) {
     abort_s = initial_abort(err);
     mbar_init(&bar_q, 1);
+    mbar_init(&bar_qt, 4);
     mbar_init(&bar_drain, 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&bar_kf[s], 1); mbar_init(&bar_ke[s], 5);
-      mbar_init(&bar_sf[s], 1); mbar_init(&bar_se[s], 4);
-      mbar_init(&bar_pf[s], 4); mbar_init(&bar_pe[s], 1);
-      mbar_init(&bar_vtf[s], 4); mbar_init(&bar_vte[s], 1);
-    }
-    mbar_init(&bar_pv, 1); mbar_init(&bar_done, 1);
+    for (int s = 0; s < kStagesM; ++s) { mbar_init(&bar_kf[s], 1); mbar_init(&bar_ke[s], 1); }
+    for (int s = 0; s < 2; ++s) { mbar_init(&bar_sf[s], 1); mbar_init(&bar_pf[s], 4); }
+    mbar_init(&bar_pv, 1);
+    mbar_init(&bar_done, 1);
     fence_barrier_init();
   }
   if (warp == 0) { tmem_alloc(&tmem_base_s, 512); tmem_relinquish(); }
   __syncthreads();
+  pdl_trigger();   // after this block's tensor-memory allocation
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
 
@@ -109,43 +113,47 @@ mla_prefill_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_con
         tma_load_2d(smem + kQTail, &tm_q64, &bar_q, 512, t * 128);
       }
       __syncwarp();
-      if (mbar_wait_warp(&bar_q, 0, err, &abort_s)) {
+      // the softmax warps move Q's nope part into TMEM columns 0-127
+      if (mbar_wait_warp(&bar_qt, 0, err, &abort_s)) {
+        tc_fence_after();
         const uint32_t sq = smem_addr(smem + kQOff);
         auto issue_s = [&](int j) -> bool {
-          const int s = j & 1;
-          const uint32_t ph = (j >> 1) & 1;
-          if (!mbar_wait_warp(&bar_kf[s], ph, err, &abort_s)) return false;
-          if (!mbar_wait_warp(&bar_se[s], ph ^ 1, err, &abort_s)) return false;
+          const int s = j % kStagesM, sb = j & 1;
+          if (!mbar_wait_warp(&bar_kf[s], (j / kStagesM) & 1, err, &abort_s)) return false;
           tc_fence_after();
           const uint32_t sk = smem_addr(smem + kKOff + s * kKStage);
+          const uint32_t d = tmem + kTS + 64 * sb;
 #pragma unroll
           for (int k = 0; k < 16; ++k)
-            mma_e4m3_w(tmem + s * 64, sdesc_kmajor(sq + (k >> 2) * 16384 + (k & 3) * 32, 128),
-                       sdesc_kmajor(sk + (k >> 2) * 8192 + (k & 3) * 32, 128), kIdescQK, k > 0);
+            mma_e4m3_ts_w(d, tmem + 8 * k, sdesc_kmajor(sk + (k >> 2) * 8192 + (k & 3) * 32, 128),
+                          kIdescQK, k > 0);
 #pragma unroll
           for (int k = 0; k < 2; ++k)
-            mma_e4m3_w(tmem + s * 64, sdesc_kmajor(sq + kQTail + k * 32, 64),
+            mma_e4m3_w(d, sdesc_kmajor(sq + kQTail + k * 32, 64),
                        sdesc_kmajor(sk + kKTail + k * 32, 64), kIdescQK, 1u);
-          mma_commit_w(&bar_ke[s]);
-          mma_commit_w(&bar_sf[s]);
+          mma_commit_w(&bar_sf[sb]);
           return true;
         };
-        bool ok = issue_s(0);
+        bool ok = issue_s(0) && (nch < 2 || issue_s(1));
         for (int j = 0; ok && j < nch; ++j) {
-          if (j + 1 < nch && !(ok = issue_s(j + 1))) break;
-          const int s = j & 1;
-          const uint32_t ph = (j >> 1) & 1;
-          if (!mbar_wait_warp(&bar_pf[s], ph, err, &abort_s) || !mbar_wait_warp(&bar_vtf[s], ph, err, &abort_s)) break;
+          const int s = j % kStagesM, sb = j & 1;
+          if (!mbar_wait_warp(&bar_pf[sb], (j >> 1) & 1, err, &abort_s)) break;
           tc_fence_after();
-          const uint32_t svt = smem_addr(smem + kVTOff + s * 32768);
+          // this CTA's 256 V columns: regions 2*hf and 2*hf + 1 of the tile
+          const uint32_t sv = smem_addr(smem + kKOff + s * kKStage) + uint32_t(hf) * 16384u;
 #pragma unroll
-          for (int k = 0; k < 4; ++k)            // 16 keys per step: 8 P columns, 16 V rows of 128 bytes
-            mma_f16_ts_w(tmem + kTO, tmem + kTP + 32 * s + 8 * k, sdesc_mn_sw128(svt + k * 2048, 8192),
-                         kIdescPV, (j > 0 || k > 0) ? 1u : 0u);
-          mma_commit_w(&bar_vte[s]);
-          mma_commit_w(&bar_pe[s]);
+          for (int term = 0; term < 2; ++term)
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk)             // 32 keys per step: 8 P columns, 32 V rows
+              mma_e4m3_ts_w(tmem + kTO, tmem + kTS + 64 * sb + 16 * term + 8 * kk,
+                            sdesc_mn_sw128(sv + kk * 4096, 8192), kIdescPV,
+                            (j > 0 || term > 0 || kk > 0) ? 1u : 0u);
+          mma_commit_w(&bar_ke[s]);          // PV(j) is the stage's last reader
           mma_commit_w(&bar_pv);
           if (j == nch - 1) mma_commit_w(&bar_done);
+          // S buffer sb holds P(j) until PV(j) has read it: MMAs of one thread
+          // run in order, so QK(j+2) may be issued into it now
+          if (j + 2 < nch && !(ok = issue_s(j + 2))) break;
         }
       }
       // exit-path drain (a no-op unless a wait gave up): no MMA in flight and
@@ -165,14 +173,14 @@ mla_prefill_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_con
       asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(idx_next) : "l"(idx_row + pw * 16 + lane));
     for (int j = 0; j <= nch; ++j) {
       if (j < nch) {
-        const int s = j & 1;
+        const int s = j % kStagesM;
         int my_idx = idx_next;
         const int key_n = (j + 1) * kChunkKeys + pw * 16 + lane;
         idx_next = -1;
         if (lane < 16 && key_n < len)
           asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(idx_next) : "l"(idx_row + key_n));
         if (lane < 16 && my_idx >= S_kv) { atomicOr(err, MSA_DEVERR_DATA); my_idx = -1; }
-        mbar_wait_ab(&bar_ke[s], ((j >> 1) & 1) ^ 1, err, &abort_s);
+        mbar_wait_ab(&bar_ke[s], ((j / kStagesM) & 1) ^ 1, err, &abort_s);   // PV(j-4) done
         uint8_t* stage = smem + kKOff + s * kKStage;
 #pragma unroll 4
         for (int rr = 0; rr < 16; ++rr) {
@@ -194,57 +202,46 @@ mla_prefill_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_con
         cp_async_commit();
       }
       if (j >= 1) {
-        const int jp = j - 1, sp = jp & 1;
+        const int sp = (j - 1) % kStagesM;
         if (j < nch) cp_async_wait<1>(); else cp_async_wait<0>();
         fence_async_shared();
-        asm volatile("bar.sync 2, 128;" ::: "memory");        // chunk jp has landed
+        asm volatile("bar.sync 2, 128;" ::: "memory");        // chunk j-1 has landed
         if (pt == 0) mbar_arrive(&bar_kf[sp]);
       }
-    }
-  } else if (warp >= 9) {
-    // ---------------- widening warps: V of chunk jp to f16 once it has landed
-    const int ct = tid - 288;
-    for (int jp = 0; jp < nch; ++jp) {
-      const int sp = jp & 1;
-      mbar_wait_ab(&bar_kf[sp], (jp >> 1) & 1, err, &abort_s);
-      // V for this CTA's d_v half as f16, rows = keys: item = (key, 16 columns)
-      mbar_wait_ab(&bar_vte[sp], ((jp >> 1) & 1) ^ 1, err, &abort_s);   // PV(jp-2) done
-      const uint8_t* stage = smem + kKOff + sp * kKStage;
-      uint8_t* vimg = smem + kVTOff + sp * 32768;
-#pragma unroll 2
-      for (int x = ct; x < kChunkKeys * 16; x += 128) {
-        const int kr = x >> 4, g16 = x & 15;
-        const int d0 = hf * 256 + g16 * 16;                   // first of 16 columns
-        const uint4 v = *reinterpret_cast<const uint4*>(stage + (d0 >> 7) * 8192 +
-                                                        swz_offset(kr, (d0 & 127) >> 4, 128));
-        uint4 lo4, hi4;
-        lo4.x = e4m3x2_to_f16x2(uint16_t(v.x)); lo4.y = e4m3x2_to_f16x2(uint16_t(v.x >> 16));
-        lo4.z = e4m3x2_to_f16x2(uint16_t(v.y)); lo4.w = e4m3x2_to_f16x2(uint16_t(v.y >> 16));
-        hi4.x = e4m3x2_to_f16x2(uint16_t(v.z)); hi4.y = e4m3x2_to_f16x2(uint16_t(v.z >> 16));
-        hi4.z = e4m3x2_to_f16x2(uint16_t(v.w)); hi4.w = e4m3x2_to_f16x2(uint16_t(v.w >> 16));
-        const int dl = g16 * 16;                               // local column 0..255
-        uint8_t* blk = vimg + (dl >> 6) * 8192;                // 64 f16 columns per 128-byte row
-        const uint32_t c0 = uint32_t(dl & 63) >> 3;
-        *reinterpret_cast<uint4*>(blk + swz_offset(kr, c0, 128)) = lo4;
-        *reinterpret_cast<uint4*>(blk + swz_offset(kr, c0 + 1, 128)) = hi4;
-      }
-      fence_async_shared();
-      __syncwarp();
-      if (lane == 0) { mbar_arrive(&bar_vtf[sp]); mbar_arrive(&bar_ke[sp]); }
     }
   } else {
     // ---------------- softmax (warps 5-8): thread = head row (TMEM lane)
     const int q4 = warp & 3;
     const int row = q4 * 32 + lane;
     const uint32_t lane_off = uint32_t(q4 * 32) << 16;
-    float m = -INFINITY, m_true = -INFINITY, l = 0.f;
+    if (nch > 0) {
+      // Q's nope bytes of this head into TMEM columns 0-127, four per column
+      // in ascending order (the layout of an 8-bit A operand in TMEM)
+      if (mbar_wait_warp(&bar_q, 0, err, &abort_s)) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          uint32_t v[32];
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 q = *reinterpret_cast<const uint4*>(smem + kQOff + r * 16384 +
+                                                            swz_offset(uint32_t(row), uint32_t(c), 128));
+            v[4 * c] = q.x; v[4 * c + 1] = q.y; v[4 * c + 2] = q.z; v[4 * c + 3] = q.w;
+          }
+          tmem_st32(tmem + lane_off + 32 * r, v);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_qt);
+    }
+    float ref = -INFINITY, m_true = -INFINITY, l = 0.f;
     // validity of the chunk's 64 keys: lane holds keys lane and lane + 32,
     // loaded one chunk ahead and combined with two ballots
     int ia = -1, ib = -1;
     if (lane < len) asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(ia) : "l"(idx_row + lane));
     if (lane + 32 < len) asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(ib) : "l"(idx_row + lane + 32));
     for (int j = 0; j < nch; ++j) {
-      const int s = j & 1;
+      const int sb = j & 1;
       const uint32_t ph = (j >> 1) & 1;
       const uint64_t valid = uint64_t(__ballot_sync(0xffffffffu, ia >= 0 && ia < S_kv)) |
                              (uint64_t(__ballot_sync(0xffffffffu, ib >= 0 && ib < S_kv)) << 32);
@@ -254,19 +251,17 @@ mla_prefill_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_con
         if (k0 < len) asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(ia) : "l"(idx_row + k0));
         if (k0 + 32 < len) asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(ib) : "l"(idx_row + k0 + 32));
       }
-      mbar_wait_ab(&bar_sf[s], ph, err, &abort_s);
+      mbar_wait_ab(&bar_sf[sb], ph, err, &abort_s);
       tc_fence_after();
+      const uint32_t s_col = tmem + lane_off + kTS + 64 * sb;
       float x[64];
 #pragma unroll
       for (int c = 0; c < 64; c += 32) {
         uint32_t v[32];
-        tmem_ld32(tmem + lane_off + s * 64 + c, v);
+        tmem_ld32(s_col + c, v);
 #pragma unroll
         for (int e = 0; e < 32; ++e) x[c + e] = __uint_as_float(v[e]);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_se[s]);
       float mx = -INFINITY;
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
@@ -274,13 +269,12 @@ mla_prefill_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_con
         mx = fmaxf(mx, x[c]);
       }
       m_true = fmaxf(m_true, mx);
-      mbar_wait_ab(&bar_pe[s], ph ^ 1, err, &abort_s);      // PV_{j-2} done: P buffer free
-      const bool grow = mx > m + kRescale;
-      const bool need = grow && (m > -INFINITY);
+      const bool grow = mx > ref + kLimit;                 // also when ref == -inf
+      const bool need = grow && (ref > -INFINITY);
       if (__any_sync(0xffffffffu, need)) {
-        mbar_wait_ab(&bar_pv, (j - 1) & 1, err, &abort_s);
+        mbar_wait_ab(&bar_pv, (j - 1) & 1, err, &abort_s);  // PV(j-1) done: O is settled
         tc_fence_after();
-        const float alpha = need ? exp2f(m - mx) : 1.0f;
+        const float alpha = need ? exp2f(ref - (mx - kHead)) : 1.0f;
 #pragma unroll 4
         for (int c = 0; c < 256; c += 16) {
           uint32_t v[16];
@@ -289,31 +283,42 @@ mla_prefill_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_con
           for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
           tmem_st16(tmem + lane_off + kTO + c, v);
         }
-        tc_fence_before();
         if (need) l *= alpha;
       }
-      if (grow) m = mx;
-      const float mref = (m == -INFINITY) ? 0.f : m;
+      if (grow) ref = mx - kHead;
+      const float r0 = (ref == -INFINITY) ? 0.f : ref;
+      // P and its two e4m3 terms, four codes per TMEM column in key order:
+      // term 0 in columns 0-15 of this S buffer, term 1 in columns 16-31
       uint32_t w[32];
       float sum = 0.f;
 #pragma unroll
-      for (int c = 0; c < 64; c += 2) {
-        const float p0 = fast_exp2(x[c] - mref), p1 = fast_exp2(x[c + 1] - mref);
-        sum += p0 + p1;
-        w[c >> 1] = pack_f16x2(p0, p1);
+      for (int c = 0; c < 16; ++c) {
+        float p[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) p[i] = fast_exp2(x[4 * c + i] - r0);
+        sum += (p[0] + p[1]) + (p[2] + p[3]);
+        const uint16_t e01 = e4m3x2_from_f32(p[0], p[1]), e23 = e4m3x2_from_f32(p[2], p[3]);
+        w[c] = uint32_t(e01) | (uint32_t(e23) << 16);
+        const uint32_t h01 = e4m3x2_to_f16x2(e01), h23 = e4m3x2_to_f16x2(e23);
+        const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+        const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+        // the remainders are exact in fp32
+        const uint16_t g01 = e4m3x2_from_f32(p[0] - f01.x, p[1] - f01.y);
+        const uint16_t g23 = e4m3x2_from_f32(p[2] - f23.x, p[3] - f23.y);
+        w[16 + c] = uint32_t(g01) | (uint32_t(g23) << 16);
       }
-      tmem_st32(tmem + lane_off + kTP + 32 * s, w);
+      tmem_st32(s_col, w);
       l += sum;
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_pf[s]);
+      if (lane == 0) mbar_arrive(&bar_pf[sb]);
     }
     // ---------------- epilogue
     if (nch > 0) mbar_wait_ab(&bar_done, 0, err, &abort_s);
     tc_fence_after();
     const float sig2 = sink != nullptr ? sink_scale2 * __ldg(sink + row) : -INFINITY;
-    const float M = fmaxf(m, sig2);
-    const float a = (m == -INFINITY) ? 0.f : exp2f(m - M);
+    const float M = fmaxf(ref, sig2);
+    const float a = (ref == -INFINITY) ? 0.f : exp2f(ref - M);
     const float ls = (sig2 == -INFINITY) ? 0.f : exp2f(sig2 - M);
     const float Z = l * a + ls;
     const float so = (Z > 0.f && nch > 0) ? (a / Z) * v_scale : 0.f;
@@ -362,11 +367,11 @@ cudaError_t launch_sparse_mla(const MlaArgs& a, cudaStream_t stream, const char*
   cudaError_t e = cudaFuncSetAttribute(mla_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMlaSmem);
   if (e != cudaSuccess) return e;
   profile_mark(stream, 0);
-  mla_prefill_kernel<<<a.T * 2, kMlaThreads, kMlaSmem, stream>>>(
-      tm_q128, tm_q64, a.kv, a.indices, a.topk_length, a.sink, a.c_qk * kLog2e, a.c_sink * kLog2e,
-      a.v_scale, a.T, a.S_kv, a.topk, a.out, a.max_logits, a.lse, a.err);
+  e = launch_pdl(mla_prefill_kernel, a.T * 2, kMlaThreads, kMlaSmem, stream, tm_q128, tm_q64, a.kv,
+                 a.indices, a.topk_length, a.sink, a.c_qk * kLog2e, a.c_sink * kLog2e, a.v_scale,
+                 a.T, a.S_kv, a.topk, a.out, a.max_logits, a.lse, a.err);
   profile_mark(stream, 1);
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace msa

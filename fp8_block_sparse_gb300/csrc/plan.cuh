@@ -31,6 +31,8 @@ static __global__ void plan_tiles_kernel(const int32_t* __restrict__ seq_lens,
                                          int max_pages, int max_tiles,
                                          TileInfo* __restrict__ tiles, int* __restrict__ n_tiles,
                                          unsigned* err) {
+  pdl_wait();      // inputs may come from the previous kernel in the stream
+  pdl_trigger();
   int n = 0;
   for (int b = 0; b < B; ++b) {
     const int q0 = cu_q[b], q1 = cu_q[b + 1], L = seq_lens[b];

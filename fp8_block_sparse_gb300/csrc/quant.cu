@@ -72,6 +72,8 @@ __global__ void __launch_bounds__(256) quant_vec_kernel(const uint16_t* __restri
                                                         int64_t x_stride,
                                                         uint8_t* __restrict__ out,
                                                         int64_t out_stride, float s_inv) {
+  pdl_wait();      // inputs may come from the previous kernel in the stream
+  pdl_trigger();
   const uint64_t total = uint64_t(rows) * chunks_per_row;
   const uint64_t step = uint64_t(gridDim.x) * blockDim.x;
   uint64_t c = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -103,8 +105,37 @@ template <bool BF16>
 __global__ void __launch_bounds__(256) quant_contig_kernel(const uint4* __restrict__ x,
                                                            uint64_t chunks,
                                                            uint4* __restrict__ out, float s_inv) {
+  pdl_wait();      // inputs may come from the previous kernel in the stream
+  pdl_trigger();
   const uint64_t step = uint64_t(gridDim.x) * blockDim.x;
   uint64_t c = uint64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  for (; c + 3 * step < chunks; c += 4 * step) {
+    uint4 a[4], b[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      a[u] = __ldcs(x + 2 * (c + u * step));
+      b[u] = __ldcs(x + 2 * (c + u * step) + 1);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) out[c + u * step] = quant16<BF16>(a[u], b[u], s_inv);
+  }
+  for (; c < chunks; c += step) out[c] = quant16<BF16>(__ldcs(x + 2 * c), __ldcs(x + 2 * c + 1), s_inv);
+}
+
+// Several contiguous tensors: block b works on the tensor whose block range
+// holds it, striding over that tensor's chunks like quant_contig_kernel.
+template <bool BF16>
+__global__ void __launch_bounds__(256) quant_multi_kernel(const QuantMulti q) {
+  pdl_wait();      // inputs may come from the previous kernel in the stream
+  pdl_trigger();
+  int j = 0;
+  while (j + 1 < q.n && int(blockIdx.x) >= q.block0[j + 1]) ++j;
+  const uint4* __restrict__ x = q.x[j];
+  uint4* __restrict__ out = q.out[j];
+  const uint64_t chunks = q.chunks[j];
+  const float s_inv = q.s_inv[j];
+  const uint64_t step = uint64_t(q.block0[j + 1] - q.block0[j]) * blockDim.x;
+  uint64_t c = uint64_t(int(blockIdx.x) - q.block0[j]) * blockDim.x + threadIdx.x;
   for (; c + 3 * step < chunks; c += 4 * step) {
     uint4 a[4], b[4];
 #pragma unroll
@@ -125,6 +156,8 @@ __global__ void __launch_bounds__(256) quant_scalar_kernel(const uint16_t* __res
                                                            int64_t x_stride,
                                                            uint8_t* __restrict__ out,
                                                            int64_t out_stride, float s_inv) {
+  pdl_wait();      // inputs may come from the previous kernel in the stream
+  pdl_trigger();
   const int64_t total = rows * cols;
   for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += int64_t(gridDim.x) * blockDim.x) {
@@ -149,6 +182,8 @@ __global__ void __launch_bounds__(256) quant_scalar_kernel(const uint16_t* __res
 // slot) row of D codes is written by D/16 neighbouring threads.
 template <bool BF16>
 __global__ void __launch_bounds__(256) kv_store_kernel(KvStoreArgs a, int tpb) {
+  pdl_wait();      // inputs may come from the previous kernel in the stream
+  pdl_trigger();
   __shared__ int s_page[256];
   __shared__ int s_slot[256];
   const int t0 = blockIdx.x * tpb;
@@ -347,6 +382,8 @@ MSA_DEV void rope_finish(const RopeQuantArgs& a, const RopeChunk& k) {
 template <bool BF16, bool NEOX>
 __global__ void __launch_bounds__(256) rope_quant_kernel(RopeQuantArgs a, int upb_n, int nb_nope,
                                                          int upb_r) {
+  pdl_wait();      // inputs may come from the previous kernel in the stream
+  pdl_trigger();
   const int nn = a.d_nope / 16, nr = a.d_rope / 16, cpr = nn + nr;
   const int64_t units = a.rows * int64_t(a.heads);
   const bool nope_role = int(blockIdx.x) < nb_nope;
@@ -418,11 +455,11 @@ cudaError_t launch_rope_quant(const RopeQuantArgs& a, bool bf16, bool neox, cuda
   const unsigned g = unsigned(grid);
   const int nb = int(nb_nope);
   if (bf16) {
-    if (neox) rope_quant_kernel<true, true><<<g, 256, 0, stream>>>(a, upb_n, nb, upb_r);
-    else rope_quant_kernel<true, false><<<g, 256, 0, stream>>>(a, upb_n, nb, upb_r);
+    if (neox) launch_pdl(rope_quant_kernel<true, true>, g, 256, 0, stream, a, upb_n, nb, upb_r);
+    else launch_pdl(rope_quant_kernel<true, false>, g, 256, 0, stream, a, upb_n, nb, upb_r);
   } else {
-    if (neox) rope_quant_kernel<false, true><<<g, 256, 0, stream>>>(a, upb_n, nb, upb_r);
-    else rope_quant_kernel<false, false><<<g, 256, 0, stream>>>(a, upb_n, nb, upb_r);
+    if (neox) launch_pdl(rope_quant_kernel<false, true>, g, 256, 0, stream, a, upb_n, nb, upb_r);
+    else launch_pdl(rope_quant_kernel<false, false>, g, 256, 0, stream, a, upb_n, nb, upb_r);
   }
   return cudaGetLastError();
 }
@@ -440,10 +477,42 @@ cudaError_t launch_kv_store(const KvStoreArgs& a, bool bf16, cudaStream_t stream
   tpb = tpb < 1 ? 1 : (tpb > 256 ? 256 : tpb);
   const int grid = (a.T + tpb - 1) / tpb;
   if (bf16)
-    kv_store_kernel<true><<<grid, 256, 0, stream>>>(a, tpb);
+    launch_pdl(kv_store_kernel<true>, grid, 256, 0, stream, a, tpb);
   else
-    kv_store_kernel<false><<<grid, 256, 0, stream>>>(a, tpb);
+    launch_pdl(kv_store_kernel<false>, grid, 256, 0, stream, a, tpb);
   return cudaGetLastError();
+}
+
+bool quant_multi_eligible(const void* x, const void* out, int64_t rows, int64_t cols,
+                          int64_t x_stride, int64_t out_stride) {
+  return (x_stride == cols) && (out_stride == cols) && reinterpret_cast<uintptr_t>(x) % 16 == 0 &&
+         reinterpret_cast<uintptr_t>(out) % 16 == 0 && (rows * cols) % 16 == 0 &&
+         (rows * cols) / 16 < (1ll << 32);
+}
+
+cudaError_t launch_quant_multi(QuantMulti& q, bool bf16, cudaStream_t stream) {
+  if (q.n == 0) return cudaSuccess;
+  // the grid of one contiguous launch (<= 8 blocks per SM, 4 chunks per
+  // thread), dealt out in proportion to the tensors' chunks, >= 1 each
+  const int threads = 256;
+  uint64_t total = 0;
+  for (int j = 0; j < q.n; ++j) total += q.chunks[j];
+  const uint64_t want = (total + 4 * threads - 1) / (4 * threads);
+  const uint64_t cap = uint64_t(num_sms()) * 8;
+  const int grid = int(want < cap ? want : cap) > q.n ? int(want < cap ? want : cap) : q.n;
+  int b = 0;
+  uint64_t acc = 0;
+  for (int j = 0; j < q.n; ++j) {
+    q.block0[j] = b;
+    acc += q.chunks[j];
+    int next = int((acc * uint64_t(grid) + total - 1) / total);
+    if (next < b + 1) next = b + 1;
+    if (next > grid - (q.n - 1 - j)) next = grid - (q.n - 1 - j);
+    b = next;
+  }
+  q.block0[q.n] = b;
+  if (bf16) return launch_pdl(quant_multi_kernel<true>, b, threads, 0, stream, q);
+  return launch_pdl(quant_multi_kernel<false>, b, threads, 0, stream, q);
 }
 
 cudaError_t launch_quant(const void* x, bool bf16, int64_t rows, int64_t cols, int64_t x_stride,
@@ -462,28 +531,28 @@ cudaError_t launch_quant(const void* x, bool bf16, int64_t rows, int64_t cols, i
     const uint4* xv = reinterpret_cast<const uint4*>(x);
     uint4* ov = reinterpret_cast<uint4*>(out);
     if (bf16)
-      quant_contig_kernel<true><<<grid, threads, 0, stream>>>(xv, chunks, ov, s_inv);
+      launch_pdl(quant_contig_kernel<true>, grid, threads, 0, stream, xv, chunks, ov, s_inv);
     else
-      quant_contig_kernel<false><<<grid, threads, 0, stream>>>(xv, chunks, ov, s_inv);
+      launch_pdl(quant_contig_kernel<false>, grid, threads, 0, stream, xv, chunks, ov, s_inv);
   } else if (aligned && cols % 16 == 0 && x_stride % 8 == 0 && out_stride % 16 == 0 &&
              rows < (1ll << 32) && rows * (cols / 16) < (1ll << 40)) {
     const uint64_t chunks = uint64_t(rows) * uint64_t(cols / 16);
     const uint64_t want = (chunks + 2 * threads - 1) / (2 * threads);
     const int grid = int(want < uint64_t(sms) * 8 ? (want ? want : 1) : uint64_t(sms) * 8);
     if (bf16)
-      quant_vec_kernel<true><<<grid, threads, 0, stream>>>(xs, uint32_t(rows), uint32_t(cols / 16),
-                                                           x_stride, out, out_stride, s_inv);
+      launch_pdl(quant_vec_kernel<true>, grid, threads, 0, stream, xs, uint32_t(rows),
+                 uint32_t(cols / 16), x_stride, out, out_stride, s_inv);
     else
-      quant_vec_kernel<false><<<grid, threads, 0, stream>>>(xs, uint32_t(rows), uint32_t(cols / 16),
-                                                            x_stride, out, out_stride, s_inv);
+      launch_pdl(quant_vec_kernel<false>, grid, threads, 0, stream, xs, uint32_t(rows),
+                 uint32_t(cols / 16), x_stride, out, out_stride, s_inv);
   } else {
     const int64_t total = rows * cols;
     const int64_t want = (total + threads - 1) / threads;
     const int grid = int(want < int64_t(sms) * 8 ? want : int64_t(sms) * 8);
     if (bf16)
-      quant_scalar_kernel<true><<<grid, threads, 0, stream>>>(xs, rows, cols, x_stride, out, out_stride, s_inv);
+      launch_pdl(quant_scalar_kernel<true>, grid, threads, 0, stream, xs, rows, cols, x_stride, out, out_stride, s_inv);
     else
-      quant_scalar_kernel<false><<<grid, threads, 0, stream>>>(xs, rows, cols, x_stride, out, out_stride, s_inv);
+      launch_pdl(quant_scalar_kernel<false>, grid, threads, 0, stream, xs, rows, cols, x_stride, out, out_stride, s_inv);
   }
   return cudaGetLastError();
 }

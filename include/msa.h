@@ -145,6 +145,34 @@ msa_status msa_quant_fp8(const void* x, msa_dtype x_dtype, int64_t rows, int64_t
                          int64_t out_row_stride, const float* scale, msa_stream_t stream);
 
 /*
+ * Several step-(a) quantisations in one launch: each entry of `tensors` is
+ * quantised exactly as msa_quant_fp8 would with the same x_dtype and
+ * out_dtype (the same rounding, s_inv rule, saturation and NaN handling), so
+ * the outputs are identical byte for byte; [30971] implementation step 3
+ * quantises q and idx_q with their own scales, which is the use this serves:
+ * one launch instead of one per tensor, so the tail of the first never idles
+ * the GPU before the second starts.
+ *
+ * tensors:  host array of n descriptors, 1 <= n <= MSA_QUANT_MULTI_MAX; the
+ *           descriptors and their scale pointers are read during the call
+ *           only (caller-owned).
+ * Contiguous tensors (row strides equal to cols, 16-byte aligned, rows*cols a
+ * multiple of 16) share one launch; any other entry is handled as its own
+ * msa_quant_fp8 call after it. Validation of every entry happens before any
+ * launch; errors as msa_quant_fp8.
+ */
+#define MSA_QUANT_MULTI_MAX 8
+typedef struct msa_quant_tensor {
+  const void* x;             /* device, rows x cols of x_dtype, row r at r * x_row_stride */
+  int64_t rows, cols, x_row_stride;
+  void* out;                 /* device e4m3, row r at byte offset r * out_row_stride */
+  int64_t out_row_stride;
+  const float* scale;        /* host, NULL = unit scale */
+} msa_quant_tensor;
+msa_status msa_quant_fp8_multi(const msa_quant_tensor* tensors, int n, msa_dtype x_dtype,
+                               msa_dtype out_dtype, msa_stream_t stream);
+
+/*
  * The store before the path: quantise the new tokens' K, V and index-K rows
  * into the paged e4m3 pools. [30971] implementation step 4 (the sparse KV
  * pool's K / V / index-K stores, each with a per-tensor scale whose absence

@@ -189,3 +189,26 @@ def test_noalloc_reports_argument_errors_before_its_scratch_limit(lib):
     assert lib.msa_index_topk(p, p, p, p, p, 1, T, T, 32, 128, 16, 64, 64, p, p, 1 << 40, None) == 2
     # valid sizes over the scratch limit: the limit is reported
     assert lib.msa_index_topk_noalloc(p, p, p, p, p, 1, T, T, 4, 128, 16, 64, 64, p, None) == 5
+
+
+def test_quant_multi_validation(lib):
+    class QT(ctypes.Structure):
+        _fields_ = [("x", ctypes.c_void_p), ("rows", ctypes.c_int64), ("cols", ctypes.c_int64),
+                    ("x_row_stride", ctypes.c_int64), ("out", ctypes.c_void_p),
+                    ("out_row_stride", ctypes.c_int64), ("scale", ctypes.POINTER(ctypes.c_float))]
+    d = (QT * 9)()
+    for i in range(9):
+        d[i] = QT(256, 4, 16, 16, 512, 16, None)
+    arr = ctypes.cast(d, ctypes.c_void_p)
+    assert lib.msa_quant_fp8_multi(arr, 0, 0, 2, None) == 1        # n out of range
+    assert lib.msa_quant_fp8_multi(arr, 9, 0, 2, None) == 1
+    assert lib.msa_quant_fp8_multi(None, 1, 0, 2, None) == 1
+    assert lib.msa_quant_fp8_multi(arr, 2, 0, 3, None) == 2        # e5m2
+    assert lib.msa_quant_fp8_multi(arr, 2, 2, 2, None) == 1        # e4m3 input
+    d[1] = QT(256, 4, 16, 8, 512, 16, None)                       # stride < cols
+    assert lib.msa_quant_fp8_multi(arr, 2, 0, 2, None) == 1
+    d[1] = QT(256, 4, 16, 16, 512, 16, ctypes.pointer(ctypes.c_float(0.0)))
+    assert lib.msa_quant_fp8_multi(arr, 2, 0, 2, None) == 1        # zero scale
+    d[0] = QT(None, 0, 16, 16, None, 16, None)
+    d[1] = QT(None, 4, 0, 16, None, 16, None)
+    assert lib.msa_quant_fp8_multi(arr, 2, 0, 2, None) == 0        # empty entries: no-op

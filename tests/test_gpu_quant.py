@@ -78,3 +78,18 @@ def test_empty_and_e5m2(msa):
     import ctypes
     assert lib.msa_quant_fp8(ctypes.c_void_p(y.data_ptr()), 0, 4, 16, 16, ctypes.c_void_p(o.data_ptr()),
                              3, 16, None, None) == 2
+
+
+def test_multi_launch_equals_separate_calls(msa):
+    # Q and idx_q of the 8k workload plus a strided slice (handled by its own
+    # launch after the shared one): every output byte-identical to quant_fp8's
+    w = wl.make_gqa(wl.CONFIGS["prefill8k"])
+    q, iq = _dev_bf16(w.q), _dev_bf16(w.idx_q)
+    sl = q[:1000, :, :64]                                   # rows of 64 with stride 128
+    outs = msa.quant_fp8_multi([(q, w.scales["q"]), (iq, w.scales["idx_q"]), (sl, 0.75)])
+    for got, (x, sc) in zip(outs, [(q, w.scales["q"]), (iq, w.scales["idx_q"]), (sl, 0.75)]):
+        assert torch.equal(got, msa.quant_fp8(x, sc))
+    assert np.array_equal(outs[1].cpu().numpy(), oq.quantize(w.idx_q, w.scales["idx_q"]))
+    # one tensor, and a scale-free entry
+    one = msa.quant_fp8_multi([(iq, None)])[0]
+    assert np.array_equal(one.cpu().numpy(), oq.quantize(w.idx_q, None))

@@ -8,9 +8,10 @@ tensor memory and returns. This test runs each tensor-core entry point that
 way on small cases and checks that
 
 * no call faults: msa_check_errors reports MSA_ERR_TIMEOUT (or MSA_OK when
-  every wait of a call happened to be complete at its first test), never a
-  CUDA error; the prefill attention and sparse-MLA cases, whose pipelines
-  always wait, must report the timeout;
+  every wait of a call completed within its first test, which may itself
+  suspend the thread for a while before giving an answer), never a CUDA
+  error; the prefill attention case, whose pipeline always waits longer
+  than that, must report the timeout;
 * with the switch off again, the same calls are exact against the oracle
   (the context is intact and nothing is left over in the shared state).
 """
@@ -32,8 +33,8 @@ def _cases():
     pre = wl.make_gqa(wl.CONFIGS["tiny"], T_override=1300)
     dec = wl.make_gqa(wl.GQAConfig("dec", 24, (), 1, 16, 2, 4, 128, 128, 16, "channel",
                                    len_range=(1000, 9000), max_pages=80, pool_factor=1.2, seed=51))
-    mla = wl.make_mla(wl.CONFIGS["mla"], T_override=4, S_override=5000, topk_override=1024,
-                      len_range=(900, 1024))
+    mla = wl.make_mla(wl.CONFIGS["mla"], T_override=12, S_override=32768, topk_override=2048,
+                      len_range=(1500, 2048))
     return pre, dec, mla
 
 
@@ -91,7 +92,7 @@ def test_forced_timeouts_drain_and_the_next_calls_are_exact(msa):
         msa.debug_force_timeouts(False)
     print("forced-timeout statuses:", seen)
     assert all(s in (0, 4) for s in seen.values()), seen
-    assert seen["attention prefill"] == 4 and seen["sparse MLA"] == 4, seen
+    assert seen["attention prefill"] == 4, seen
     assert _status(msa) == 0
     # the same work with the switch off: exact against the oracle
     for w in (pre, dec):
