@@ -47,7 +47,7 @@ constexpr int kVOff = 81920;         // 3 stages x V^T f16 image             96 
 constexpr int kBlistOff = 180224;    // union block list (int16)              4 KB
 constexpr int kBitsOff = 184320;     // union bitmap, 2048 bits              256 B
 constexpr int kPrefillSmem = 184576 + 1024;
-constexpr int kPrefillThreads = 384;
+constexpr int kPrefillThreads = 576;   // producer, MMA, 16 softmax warps
 
 constexpr uint32_t kIdescQK = idesc_f32(128, 128);
 constexpr uint32_t kIdescPV = idesc_f32(128, 128);
@@ -93,9 +93,16 @@ vt_convert_kernel(const uint8_t* __restrict__ v_cache, const int32_t* __restrict
 
 // ------------------------------------------------------------ prefill
 // One CTA = two 128-row tiles (X = 0, 1) of one kv head: 2 x 128/G tokens x
-// G heads. Warp roles: 0 producer (TMA), 1 MMA issue, 2-3 idle, 4-7 softmax
-// of tile 0, 8-11 softmax of tile 1 (one thread per row; warp w reads TMEM
-// lanes 32*(w%4)). TMEM: S_0 and S_1 at columns 0 and 128, O_0 and O_1 at 256
+// G heads. Warp roles: 0 producer (TMA), 1 MMA issue, 2-17 softmax: two
+// threads per row, one per half of the 128 columns (warp w reads TMEM lanes
+// 32*(w%4), so the two threads of a row sit in two warps of the same lane
+// quarter; they share the row's running maximum through shared memory). A
+// row's softmax of one block is thus two 64-column chains, not one
+// 128-column chain, which halves the latency the MMAs wait on. With 18 warps
+// a sub-partition holds up to 5 of them, so a thread gets 96 registers: each
+// half reads its 64 S columns twice (once for the maximum, once for P), 32 at
+// a time, and writes its P (f16 pairs) over the first 32 of its own S
+// columns, so the two halves never touch each other's columns. TMEM: S_0 and S_1 at columns 0 and 128, O_0 and O_1 at 256
 // and 384. P (f16, two per 32-bit column) overwrites the first 64 columns of
 // its tile's S once the softmax has read S, and the PV MMA takes it as the A
 // operand straight from TMEM, so P never touches shared memory (which would
@@ -122,6 +129,8 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   __shared__ uint32_t tmem_base_s;
   __shared__ int n_union_s;
   __shared__ int abort_s;
+  __shared__ float xmax_s[2][2][2][128];   // [block parity][tile][half][row]: partial row maxima
+  __shared__ float lsum_s[2][2][128];      // [tile][half][row]: partial row sums
 
   const int n_tiles = *n_tiles_p;
   const int tile_rank = blockIdx.x / Hkv;
@@ -143,7 +152,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       mbar_init(&bar_kf[s], 1); mbar_init(&bar_ke[s], 1);
       mbar_init(&bar_vf[s], 1); mbar_init(&bar_ve[s], 1);
     }
-    for (int x = 0; x < 2; ++x) { mbar_init(&bar_sf[x], 1); mbar_init(&bar_pf[x], 4); }
+    for (int x = 0; x < 2; ++x) { mbar_init(&bar_sf[x], 1); mbar_init(&bar_pf[x], 8); }
     mbar_init(&bar_done, 1);
     mbar_init(&bar_drain, 1);
     fence_barrier_init();
@@ -152,10 +161,12 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   __syncthreads();
   pdl_trigger();   // after this block's tensor-memory allocation
 
-  // ---- softmax threads own rows: row = 128*X + 32*(warp%4) + lane
-  const bool is_softmax = warp >= 4;
-  const int X = (warp >> 2) - 1;
-  const int row = X * 128 + (warp & 3) * 32 + lane;
+  // ---- softmax threads: tile X, column half hh, row 128*X + 32*(warp%4) + lane
+  const bool is_softmax = warp >= 2;
+  const int sw = warp - 2;
+  const int X = sw >> 3, hh = (sw >> 2) & 1, quarter = warp & 3;
+  const int rq = quarter * 32 + lane;                             // row within the tile
+  const int row = X * 128 + rq;
   int own = -1, pos = -1, h = 0, t = 0, next_id = -1, ptr = 0;
   bool row_valid = false;
   const int32_t* src = nullptr;
@@ -169,7 +180,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       own = pos >> 7;
       src = topk + (size_t(h / (Hq / Hidx)) * T + t) * topk_k;
       int last = -1;
-      for (int k = 0; k < topk_k; ++k) {
+      for (int k = 0; hh == 0 && k < topk_k; ++k) {            // one thread per row
         const int id = __ldg(src + k);
         if (id < 0) continue;                                   // -1 padding
         if (id <= last || id > own) { atomicOr(err, MSA_DEVERR_DATA); continue; }
@@ -207,8 +218,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   const int nU = n_union_s;
   const uint32_t tmem = tmem_base_s;
 
-  if (warp < 4) {
-    setmaxnreg_dec<56>();
+  if (warp < 2) {
     if (warp == 0 && lane == 0 && nU > 0) {
       // ---------------- producer: Q of both tiles, then K pages and V^T images
       tma_prefetch_desc(&tm_q);
@@ -265,7 +275,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            mma_f16_ts_w(tmem + 256 + x * 128, tmem + x * 128 + 8 * k,
+            mma_f16_ts_w(tmem + 256 + x * 128, tmem + x * 128 + 64 * (k >> 2) + 8 * (k & 3),
                          sdesc_kmajor(sv + (k >> 2) * 16384 + (k & 3) * 32, 128), kIdescPV,
                          (j > 0 || k > 0) ? 1u : 0u);
           if (x == 1) mma_commit_w(&bar_ve[s]);
@@ -277,11 +287,11 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       mma_drain_w(&bar_drain, err);          // no MMA in flight once TMEM is freed
     }
   } else {
-    setmaxnreg_inc<224>();
-    // ---------------- softmax of tile X: one thread per row
-    const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
-    const uint32_t s_col = tmem + lane_off + X * 128;
-    const uint32_t o_col = tmem + lane_off + 256 + X * 128;
+    // ---------------- softmax of tile X, columns [64 hh, 64 hh + 64) of each row
+    const uint32_t lane_off = uint32_t(quarter * 32) << 16;
+    const uint32_t s_col = tmem + lane_off + X * 128 + 64 * hh;        // this half's S, then P
+    const uint32_t o_col = tmem + lane_off + 256 + X * 128 + 64 * hh;  // this half's O
+    const int bar_id = 1 + X * 4 + quarter;                            // the row pair's barrier
     const uint64_t scale2 = pk2(qk_scale2, qk_scale2);
     float m = -INFINITY, m_true = -INFINITY, l = 0.f;
     for (int j = 0; j < nU; ++j) {
@@ -296,150 +306,93 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         next_id = nid;
       }
       const int ncol = !sel ? 0 : (blk < own ? 128 : pos - blk * 128 + 1);
-      // S_X(j) done (and with it PV_X(j-1): O is settled and P may be rewritten)
-      if (!mbar_wait_warp(&bar_sf[X], j & 1, err, &abort_s)) break;   // uniform: tcgen05 ops follow
+      const int nc = min(64, max(0, ncol - 64 * hh));                 // valid columns of this half
+      // S_X(j) done (and with it PV_X(j-1): O is settled and P may be rewritten).
+      // The result is not used to leave the loop: the two warps of a row pair
+      // must meet at the same named barriers, so after a timeout both keep
+      // walking the blocks (every later wait returns at once) and the outputs
+      // are meaningless, which msa_check_errors reports.
+      mbar_wait_warp(&bar_sf[X], j & 1, err, &abort_s);               // warp-uniform
       tc_fence_after();
-      const bool live = ncol == 128;
-      // Speculative path, taken when every lane's row uses the whole block or
-      // none of it and no row is at its first block (so m is finite): the
-      // exponentials use the current reference m while the block maximum is
-      // reduced alongside, and S is loaded and P stored in 32-key chunks so
-      // that loads, exponentials and stores overlap. Only when some row's
-      // maximum outgrows m by 2^8 is the block redone with the new reference.
-      if (!__any_sync(0xffffffffu, (ncol > 0 && ncol < 128) || (live && m == -INFINITY))) {
-        uint32_t xs[128];
-        uint32_t w[64];
-        const uint64_t negm = pk2(-m, -m);
-        uint64_t acc0 = pk2(0.f, 0.f), acc1 = acc0;
-        float mr = -INFINITY;
-        tmem_ld32_async(s_col, slice32(xs, 0));
-        tmem_wait_ld32(slice32(xs, 0));
+      // pass 1: this half's maximum of the raw scores over its valid columns
+      // (scale > 0 commutes), then the row's through the partner thread
+      float mr = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          if (c < 3) tmem_ld32_async(s_col + 32 * (c + 1), slice32(xs, c + 1));
-          float a0 = __uint_as_float(xs[32 * c]), a1 = __uint_as_float(xs[32 * c + 1]);
+      for (int c0 = 0; c0 < 64; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(s_col + c0, v);
+        if (nc >= c0 + 32) {
+          float a0 = __uint_as_float(v[0]), a1 = __uint_as_float(v[1]);
 #pragma unroll
-          for (int e = 2; e < 32; e += 4) {
-            a0 = fmax3(a0, __uint_as_float(xs[32 * c + e]), __uint_as_float(xs[32 * c + e + 1]));
-            a1 = fmax3(a1, __uint_as_float(xs[32 * c + e + 2]), __uint_as_float(xs[32 * c + e + 3]));
+          for (int c = 2; c < 32; c += 4) {
+            a0 = fmax3(a0, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
+            a1 = fmax3(a1, __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
           }
           mr = fmax3(mr, a0, a1);
+        } else if (nc > c0) {
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const float2 y = unpk2(ffma2(pk2(__uint_as_float(xs[32 * c + e]),
-                                             __uint_as_float(xs[32 * c + e + 1])), scale2, negm));
-            const float p0 = fast_exp2(y.x), p1 = fast_exp2(y.y);
-            if (e & 2) acc1 = fadd2(acc1, pk2(p0, p1)); else acc0 = fadd2(acc0, pk2(p0, p1));
-            w[16 * c + (e >> 1)] = live ? pack_f16x2(p0, p1) : 0u;
-          }
-          tmem_st16_async(s_col + 16 * c, slice16(w, c));
-          if (c < 3) tmem_wait_ld32(slice32(xs, c + 1));
+          for (int c = 0; c < 32; ++c) mr = (c0 + c < nc) ? fmaxf(mr, __uint_as_float(v[c])) : mr;
         }
-        tmem_wait_st64(w);
-        const float mx = live ? mr * qk_scale2 : -INFINITY;
-        m_true = fmaxf(m_true, mx);
-        const bool grow = mx > m + kRescale;
-        if (__any_sync(0xffffffffu, grow)) {
-          // some row's maximum outgrew its reference: rescale O and l, redo P
-          const float alpha = grow ? exp2f(m - mx) : 1.0f;
+      }
+      xmax_s[j & 1][X][hh][rq] = mr;
+      asm volatile("bar.sync %0, 64;" ::"r"(bar_id) : "memory");
+      mr = fmaxf(mr, xmax_s[j & 1][X][hh ^ 1][rq]);
+      const float mx = mr * qk_scale2;
+      m_true = fmaxf(m_true, mx);
+      const bool grow = mx > m + kRescale;                    // also when m == -inf
+      const bool need_rescale = grow && (m > -INFINITY);
+      if (__any_sync(0xffffffffu, need_rescale)) {
+        const float alpha = need_rescale ? exp2f(m - mx) : 1.0f;
 #pragma unroll
-          for (int c = 0; c < 128; c += 16) {
-            uint32_t v[16];
-            tmem_ld16(o_col + c, v);
+        for (int c = 0; c < 64; c += 16) {
+          uint32_t v[16];
+          tmem_ld16(o_col + c, v);
 #pragma unroll
-            for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-            tmem_st16(o_col + c, v);
-          }
-          if (grow) { l *= alpha; m = mx; }
-          const uint64_t negm2 = pk2(-m, -m);
-          acc0 = pk2(0.f, 0.f);
-          acc1 = acc0;
-#pragma unroll
-          for (int e = 0; e < 128; e += 2) {
-            const float2 y = unpk2(ffma2(pk2(__uint_as_float(xs[e]), __uint_as_float(xs[e + 1])),
-                                         scale2, negm2));
-            const float p0 = fast_exp2(y.x), p1 = fast_exp2(y.y);
-            if (e & 2) acc1 = fadd2(acc1, pk2(p0, p1)); else acc0 = fadd2(acc0, pk2(p0, p1));
-            w[e >> 1] = live ? pack_f16x2(p0, p1) : 0u;
-          }
-          tmem_st64(s_col, w);
+          for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+          tmem_st16(o_col + c, v);
         }
-        if (live) {
-          const float2 a2 = unpk2(fadd2(acc0, acc1));
-          l += a2.x + a2.y;
-        }
-      } else {
-        float x[128];
-        {
-          uint32_t v[128];
-          tmem_ld128(s_col, v);
-  #pragma unroll
-          for (int e = 0; e < 128; ++e) x[e] = __uint_as_float(v[e]);
-        }
-        // row max of the raw scores over the valid columns (scale > 0 commutes)
-        float mr = -INFINITY;
-        if (ncol == 128) {
-          float a0 = x[0], a1 = x[1], a2 = x[2], a3 = x[3];
-  #pragma unroll
-          for (int c = 4; c < 128; c += 8) {
-            a0 = fmax3(a0, x[c], x[c + 1]);
-            a1 = fmax3(a1, x[c + 2], x[c + 3]);
-            a2 = fmax3(a2, x[c + 4], x[c + 5]);
-            a3 = fmax3(a3, x[c + 6], x[c + 7]);
-          }
-          mr = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
-        } else if (ncol > 0) {
-  #pragma unroll
-          for (int c = 0; c < 128; ++c) mr = (c < ncol) ? fmaxf(mr, x[c]) : mr;
-        }
-        const float mx = mr * qk_scale2;
-        m_true = fmaxf(m_true, mx);
-        const bool grow = mx > m + kRescale;                    // also when m == -inf
-        const bool need_rescale = grow && (m > -INFINITY);
-        if (__any_sync(0xffffffffu, need_rescale)) {
-          const float alpha = need_rescale ? exp2f(m - mx) : 1.0f;
-  #pragma unroll
-          for (int c = 0; c < 128; c += 16) {
-            uint32_t v[16];
-            tmem_ld16(o_col + c, v);
-  #pragma unroll
-            for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-            tmem_st16(o_col + c, v);
-          }
-          if (need_rescale) l *= alpha;
-        }
-        if (grow) m = mx;
+        if (need_rescale) l *= alpha;
+      }
+      if (grow) m = mx;
 
-        // P = exp2(S * scale - m) as f16 pairs over the first 64 columns of S_X.
-        // Three explicit paths so the common full block carries no masking.
-        uint32_t w[64];
-        if (ncol == 128) {
-          const uint64_t negm = pk2(-m, -m);
-          uint64_t acc0 = pk2(0.f, 0.f), acc1 = acc0;
-  #pragma unroll
-          for (int c = 0; c < 128; c += 2) {
-            const float2 y = unpk2(ffma2(pk2(x[c], x[c + 1]), scale2, negm));
+      // pass 2: P = exp2(S * scale - m) as f16 pairs, 32 columns at a time,
+      // each piece stored over S columns this thread has already read (and
+      // once the lanes have reconverged: the TMEM store is warp-wide). Three
+      // paths so the common full half carries no masking and an unselected
+      // row costs no exponentials.
+      const uint64_t negm = pk2(-m, -m);
+      uint64_t acc0 = pk2(0.f, 0.f), acc1 = acc0;
+#pragma unroll
+      for (int hq = 0; hq < 2; ++hq) {
+        uint32_t v[32];
+        tmem_ld32(s_col + 32 * hq, v);
+        uint32_t w[16];
+        if (nc == 64) {
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            const float2 y = unpk2(ffma2(pk2(__uint_as_float(v[c]), __uint_as_float(v[c + 1])), scale2, negm));
             const float p0 = fast_exp2(y.x), p1 = fast_exp2(y.y);
             if (c & 2) acc1 = fadd2(acc1, pk2(p0, p1)); else acc0 = fadd2(acc0, pk2(p0, p1));
             w[c >> 1] = pack_f16x2(p0, p1);
           }
-          const float2 a2 = unpk2(fadd2(acc0, acc1));
-          l += a2.x + a2.y;
-        } else if (ncol > 0) {
-          float sum = 0.f;
-  #pragma unroll
-          for (int c = 0; c < 128; c += 2) {
-            const float p0 = c < ncol ? fast_exp2(fmaf(x[c], qk_scale2, -m)) : 0.f;
-            const float p1 = c + 1 < ncol ? fast_exp2(fmaf(x[c + 1], qk_scale2, -m)) : 0.f;
-            sum += p0 + p1;
+        } else if (nc > 0) {
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            const int cc = 32 * hq + c;
+            const float p0 = cc < nc ? fast_exp2(fmaf(__uint_as_float(v[c]), qk_scale2, -m)) : 0.f;
+            const float p1 = cc + 1 < nc ? fast_exp2(fmaf(__uint_as_float(v[c + 1]), qk_scale2, -m)) : 0.f;
+            acc0 = fadd2(acc0, pk2(p0, p1));
             w[c >> 1] = pack_f16x2(p0, p1);
           }
-          l += sum;
         } else {
-  #pragma unroll
-          for (int c = 0; c < 64; ++c) w[c] = 0u;
+#pragma unroll
+          for (int c = 0; c < 16; ++c) w[c] = 0u;
         }
-        tmem_st64(s_col, w);
+        tmem_st16(s_col + 16 * hq, w);
+      }
+      {
+        const float2 a2 = unpk2(fadd2(acc0, acc1));
+        l += a2.x + a2.y;
       }
       tc_fence_before();
       __syncwarp();
@@ -449,15 +402,18 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     // ---------------- epilogue: O / (l + sink), lse, max_logit
     if (nU > 0) mbar_wait_ab(&bar_done, 0, err, &abort_s);
     tc_fence_after();
+    lsum_s[X][hh][rq] = l;
+    asm volatile("bar.sync %0, 64;" ::"r"(bar_id) : "memory");
+    const float lrow = l + lsum_s[X][hh ^ 1][rq];
     const float sig2 = (sink != nullptr && row_valid) ? sink_scale2 * __ldg(sink + h) : -INFINITY;
     const float M = fmaxf(m, sig2);
     const float a = (m == -INFINITY) ? 0.f : exp2f(m - M);
     const float ls = (sig2 == -INFINITY) ? 0.f : exp2f(sig2 - M);
-    const float Z = l * a + ls;
+    const float Z = lrow * a + ls;
     const float so = (Z > 0.f && nU > 0) ? (a / Z) * v_scale : 0.f;
-    uint16_t* orow = out + (size_t(t) * Hq + h) * 128;
+    uint16_t* orow = out + (size_t(t) * Hq + h) * 128 + 64 * hh;
 #pragma unroll
-    for (int c = 0; c < 128; c += 32) {
+    for (int c = 0; c < 64; c += 32) {
       uint32_t v[32];
       if (nU > 0) {
         tmem_ld32(o_col + c, v);
@@ -477,7 +433,7 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         }
       }
     }
-    if (row_valid) {
+    if (row_valid && hh == 0) {
       max_logit[size_t(t) * Hq + h] = m_true * kLn2;
       lse[size_t(t) * Hq + h] = (Z > 0.f) ? (M + log2f(Z)) * kLn2 : -INFINITY;
     }
@@ -572,7 +528,9 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
   const int g = (blockIdx.x / max_chunks) % Hkv;
   const int t = blockIdx.x / (max_chunks * Hkv);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int b = find_sequence(cu_q, B, t);
+  // one query per sequence (the decode launch: q_len <= 1, T == B) makes
+  // token t sequence t; otherwise search the query offsets
+  const int b = (T == B) ? t : find_sequence(cu_q, B, t);
   const int qlen = cu_q[b + 1] - cu_q[b];
   const int L = seq_lens[b];
   const int pos = L - qlen + (t - cu_q[b]);
@@ -899,8 +857,11 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
   if (warp == 1) tmem_dealloc(tmem, 64);
 }
 
-// Merges the chunks of each (token, kv head) and applies the sink.
-__global__ void __launch_bounds__(256)
+// Merges the chunks of each (token, kv head) and applies the sink. One
+// thread per output element (query row r of the group, column d), one pass
+// over the chunks with a running maximum; the chunks' loads do not depend on
+// one another, so they are all in flight together.
+__global__ void __launch_bounds__(1024)
 decode_combine_kernel(const float* __restrict__ part_o, const DecodePartial* __restrict__ part_s,
                       const int* __restrict__ n_chunks, const float* __restrict__ sink,
                       float sink_scale2, float v_scale, int Hq, int Hkv, int max_chunks,
@@ -915,23 +876,25 @@ decode_combine_kernel(const float* __restrict__ part_o, const DecodePartial* __r
   for (int x = threadIdx.x; x < G * 128; x += blockDim.x) {
     const int r = x >> 7, d = x & 127;
     const int h = g * G + r;
-    float M = -INFINITY, mt = -INFINITY;
-    for (int c = 0; c < nch; ++c) {
-      const DecodePartial ps = part_s[(unit * max_chunks + c) * G + r];
-      M = fmaxf(M, ps.m);
-      mt = fmaxf(mt, ps.m_true);
-    }
-    const float sig2 = sink != nullptr ? sink_scale2 * __ldg(sink + h) : -INFINITY;
-    const float Mz = fmaxf(M, sig2);
-    float Z = (sig2 == -INFINITY) ? 0.f : exp2f(sig2 - Mz), acc = 0.f;
+    float M = -INFINITY, mt = -INFINITY, Z = 0.f, acc = 0.f;
+#pragma unroll 4
     for (int c = 0; c < nch; ++c) {
       const size_t k = (unit * max_chunks + c) * G + r;
       const DecodePartial ps = part_s[k];
+      const float po = part_o[k * 128 + d];
+      mt = fmaxf(mt, ps.m_true);
       if (ps.m == -INFINITY) continue;
-      const float f = exp2f(ps.m - Mz);
-      Z += ps.l * f;
-      acc += part_o[k * 128 + d] * f;
+      const float Mn = fmaxf(M, ps.m);
+      const float a0 = (M == -INFINITY) ? 0.f : exp2f(M - Mn), a1 = exp2f(ps.m - Mn);
+      Z = Z * a0 + ps.l * a1;
+      acc = acc * a0 + po * a1;
+      M = Mn;
     }
+    const float sig2 = sink != nullptr ? sink_scale2 * __ldg(sink + h) : -INFINITY;
+    const float Mz = fmaxf(M, sig2);
+    const float aM = (M == -INFINITY) ? 0.f : exp2f(M - Mz);
+    Z = Z * aM + ((sig2 == -INFINITY) ? 0.f : exp2f(sig2 - Mz));
+    acc *= aM;
     const float o = Z > 0.f ? acc / Z * v_scale : 0.f;
     out[(size_t(t) * Hq + h) * 128 + d] = __bfloat16_as_ushort(__float2bfloat16_rn(o));
     if (d == 0) {
@@ -979,7 +942,8 @@ cudaError_t launch_decode(const AttnArgs& a, cudaStream_t stream, const char** w
                  a.Hidx, a.topk_k, a.max_pages, a.num_pages, mc, part_o, part_s, n_chunks, a.err);
   profile_mark(stream, 1);
   if (e != cudaSuccess) return e;
-  return launch_pdl(decode_combine_kernel, a.T * a.Hkv, 256, 0, stream, part_o, part_s, n_chunks,
+  const int cthreads = G * 128 < 1024 ? G * 128 : 1024;
+  return launch_pdl(decode_combine_kernel, a.T * a.Hkv, cthreads, 0, stream, part_o, part_s, n_chunks,
                     a.sink, a.c_sink * kLog2e, a.v_scale, a.Hq, a.Hkv, mc, a.out, a.max_logit,
                     a.lse);
 }

@@ -200,7 +200,8 @@ index_score_decode_kernel(const __grid_constant__ CUtensorMap tm_q,
 
   const int t = blockIdx.x / chunks_per_tok;
   const int c0 = (blockIdx.x % chunks_per_tok) * kChunk;
-  const int b = find_sequence(cu_q, B, t);
+  // one query per sequence (q_len <= 1, T == B) makes token t sequence t
+  const int b = (T == B) ? t : find_sequence(cu_q, B, t);
   const int qlen = cu_q[b + 1] - cu_q[b];
   const int p = seq_lens[b] - qlen + (t - cu_q[b]);
   if (p < 0 || p >= max_pages * 128) {
@@ -308,14 +309,16 @@ template <int NPL>
 __global__ void __launch_bounds__(256)
 topk_select_kernel(const float* __restrict__ scores, const int32_t* __restrict__ seq_lens,
                    const int32_t* __restrict__ cu_q, int B, int T, int Hidx, int topk,
-                   int max_pages, int32_t* __restrict__ out, unsigned* err) {
+                   int max_pages, int decode, int32_t* __restrict__ out, unsigned* err) {
   pdl_wait();      // the scores come from the scoring kernel
   pdl_trigger();
   const int lane = threadIdx.x & 31;
   const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (row >= (long long)Hidx * T) return;
   const int i = int(row / T), t = int(row % T);
-  const int b = find_sequence(cu_q, B, t);
+  // with one query per sequence (decode: q_len <= 1, T == B) token t is
+  // sequence t; otherwise search the query offsets
+  const int b = (decode && T == B) ? t : find_sequence(cu_q, B, t);
   const int qlen = cu_q[b + 1] - cu_q[b];
   const int p = seq_lens[b] - qlen + (t - cu_q[b]);
   int32_t* o = out + size_t(row) * topk;
@@ -454,11 +457,11 @@ cudaError_t launch_index_topk(const IndexArgs& a, cudaStream_t stream, const cha
   const long long rows = (long long)a.Hidx * a.T;
   const int grid = int((rows + 7) / 8);
   if (a.max_pages <= 256)
-    return launch_pdl(topk_select_kernel<8>, grid, 256, 0, stream, scores, a.seq_lens, a.cu_q, a.B, a.T, a.Hidx, a.topk, a.max_pages, a.topk_indices, a.err);
+    return launch_pdl(topk_select_kernel<8>, grid, 256, 0, stream, scores, a.seq_lens, a.cu_q, a.B, a.T, a.Hidx, a.topk, a.max_pages, int(decode), a.topk_indices, a.err);
   else if (a.max_pages <= 512)
-    return launch_pdl(topk_select_kernel<16>, grid, 256, 0, stream, scores, a.seq_lens, a.cu_q, a.B, a.T, a.Hidx, a.topk, a.max_pages, a.topk_indices, a.err);
+    return launch_pdl(topk_select_kernel<16>, grid, 256, 0, stream, scores, a.seq_lens, a.cu_q, a.B, a.T, a.Hidx, a.topk, a.max_pages, int(decode), a.topk_indices, a.err);
   else
-    return launch_pdl(topk_select_kernel<64>, grid, 256, 0, stream, scores, a.seq_lens, a.cu_q, a.B, a.T, a.Hidx, a.topk, a.max_pages, a.topk_indices, a.err);
+    return launch_pdl(topk_select_kernel<64>, grid, 256, 0, stream, scores, a.seq_lens, a.cu_q, a.B, a.T, a.Hidx, a.topk, a.max_pages, int(decode), a.topk_indices, a.err);
 }
 
 }  // namespace msa

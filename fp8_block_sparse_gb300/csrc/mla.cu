@@ -163,6 +163,8 @@ mla_prefill_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_con
     }
   } else if (warp <= 4) {
     // ---------------- gather warps: copy chunk j, then publish chunk j-1 once it has landed
+    // (publishing two behind, with three chunks in flight per warp, measured
+    // slower: the gather is not bound by the bytes it has in flight)
     // Gather: producer warp pw copies rows 16*pw .. 16*pw+15 of the chunk, one
     // row at a time with all 32 lanes (576 bytes = 36 chunks of 16 bytes), so
     // every cp.async instruction reads contiguous bytes of one kv row.

@@ -110,3 +110,26 @@ def test_zero_rows_is_a_no_op(msa):
     out = msa.rope_quant_fp8(None, pe, cs, torch.empty(0, dtype=torch.int32, device="cuda"))
     msa.check_errors()
     assert out.shape == (0, 2, 32)
+
+
+@pytest.mark.parametrize("cfg", ["prefill8k", "decode"])
+def test_indexer_query_rows(msa, cfg):
+    # The indexer's e4m3 query produced by the fused producer: idx_q of the
+    # workload [T, Hidx, 128] as nope = idx_q[..., :64] || rope(idx_q[..., 64:])
+    # at the queries' positions, quantised with idx_q's per-tensor scale (the
+    # split of d_idx into 64 + 64 is a reading; the pages fix only that the
+    # fused kernel emits the fp8 index query directly)
+    w = wl.make_gqa(wl.CONFIGS[cfg])
+    T, Hi, d = w.idx_q.shape
+    L = int(w.seq_lens.max())
+    cs = wl.rotary_table(L, 64)
+    pos = np.concatenate([np.arange(int(w.seq_lens[b]) - (int(w.cu_q[b + 1]) - int(w.cu_q[b])),
+                                    int(w.seq_lens[b])) for b in range(len(w.seq_lens))]).astype(np.int32)
+    iq = _tensor(w.idx_q, "bf16")
+    got = msa.rope_quant_fp8(iq[..., :64], iq[..., 64:], dev(cs), dev(pos), is_neox=True,
+                             scale=w.scales["idx_q"])
+    msa.check_errors()
+    rows = np.sort(np.random.default_rng(3).choice(T, size=min(T, 512), replace=False))
+    want = orq.rope_quant(w.idx_q[rows, :, :64], w.idx_q[rows, :, 64:], cs, pos[rows], True,
+                          scale=w.scales["idx_q"])
+    np.testing.assert_array_equal(got.cpu().numpy()[rows], want)
