@@ -317,21 +317,23 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       // pass 1: this half's maximum of the raw scores over its valid columns
       // (scale > 0 commutes), then the row's through the partner thread
       float mr = -INFINITY;
-#pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld32(s_col + c0, v);
-        if (nc >= c0 + 32) {
+      {
+        uint32_t v[64];
+        tmem_ld64(s_col, v);                                  // one round trip
+        if (nc == 64) {
           float a0 = __uint_as_float(v[0]), a1 = __uint_as_float(v[1]);
+          float a2 = __uint_as_float(v[2]), a3 = __uint_as_float(v[3]);
 #pragma unroll
-          for (int c = 2; c < 32; c += 4) {
+          for (int c = 4; c < 64; c += 8) {
             a0 = fmax3(a0, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
             a1 = fmax3(a1, __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
+            a2 = fmax3(a2, __uint_as_float(v[c + 4]), __uint_as_float(v[c + 5]));
+            a3 = fmax3(a3, __uint_as_float(v[c + 6]), __uint_as_float(v[c + 7]));
           }
-          mr = fmax3(mr, a0, a1);
-        } else if (nc > c0) {
+          mr = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
+        } else if (nc > 0) {
 #pragma unroll
-          for (int c = 0; c < 32; ++c) mr = (c0 + c < nc) ? fmaxf(mr, __uint_as_float(v[c])) : mr;
+          for (int c = 0; c < 64; ++c) mr = (c < nc) ? fmaxf(mr, __uint_as_float(v[c])) : mr;
         }
       }
       xmax_s[j & 1][X][hh][rq] = mr;
@@ -362,11 +364,12 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       // row costs no exponentials.
       const uint64_t negm = pk2(-m, -m);
       uint64_t acc0 = pk2(0.f, 0.f), acc1 = acc0;
+      uint32_t wp[2][16];                                     // the two P pieces
 #pragma unroll
       for (int hq = 0; hq < 2; ++hq) {
         uint32_t v[32];
         tmem_ld32(s_col + 32 * hq, v);
-        uint32_t w[16];
+        uint32_t (&w)[16] = wp[hq];
         if (nc == 64) {
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {
@@ -388,8 +391,9 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 #pragma unroll
           for (int c = 0; c < 16; ++c) w[c] = 0u;
         }
-        tmem_st16(s_col + 16 * hq, w);
+        tmem_st16_async(s_col + 16 * hq, w);
       }
+      tmem_wait_st2(wp[0], wp[1]);
       {
         const float2 a2 = unpk2(fadd2(acc0, acc1));
         l += a2.x + a2.y;
