@@ -135,35 +135,6 @@ MSA_DEV void mbar_drain_ring(uint64_t* bars, int stages, int n, unsigned* err) {
   }
 }
 
-// ---------------------------------------------------------------- clusters
-// Address of this CTA's shared variable `p` in the shared memory window of
-// cluster CTA `rank`.
-MSA_DEV uint32_t peer_smem(const void* p, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
-  return r;
-}
-// Arrive on a barrier of another CTA of the cluster (address from peer_smem).
-MSA_DEV void mbar_arrive_remote(uint32_t bar_cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster_addr)
-               : "memory");
-}
-// Bulk copy from this CTA's shared memory into another CTA's (both 16-byte
-// aligned, size a multiple of 16); completes on that CTA's barrier.
-MSA_DEV void bulk_copy_to_peer(uint32_t dst_cluster_addr, const void* src, uint32_t bytes,
-                               uint32_t bar_cluster_addr) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-          "r"(dst_cluster_addr),
-      "r"(smem_addr(src)), "r"(bytes), "r"(bar_cluster_addr)
-      : "memory");
-}
-// All threads of every CTA of the cluster.
-MSA_DEV void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
-                   "memory");
-}
-
 // ---------------------------------------------------------------- TMA
 MSA_DEV void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -196,6 +167,18 @@ MSA_DEV void cp_async16(void* dst, const void* src) {
                "l"(reinterpret_cast<uint64_t>(src))
                : "memory");
 }
+// As cp_async16, writing 16 zero bytes instead (no global read) when !valid.
+MSA_DEV void cp_async16_zfill(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(valid ? 16u : 0u)
+               : "memory");
+}
+// Arrives on `bar` once every cp.async this thread issued so far has
+// landed; the barrier's count must include these arrivals (no increment).
+MSA_DEV void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+MSA_DEV void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 MSA_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 MSA_DEV void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }

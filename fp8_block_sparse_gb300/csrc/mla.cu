@@ -13,20 +13,19 @@
 // GB300 design. The 128 heads of one query share its index list, so they are
 // the M = 128 rows of every MMA. A CTA owns one query token and one half of
 // d_v (a 128 x 512 fp32 O alone would fill all 512 TMEM columns), so both
-// halves compute S; the two CTAs of a token form a cluster and share the
-// gather: each copies half of every chunk's kv rows from global memory (the
-// scattered-row gather is the slowest part of the kernel) and hands them to
-// its peer with shared-memory-to-shared-memory bulk copies. TMEM: the 512 nope bytes of Q per head (columns 0-127,
+// halves compute S. TMEM: the 512 nope bytes of Q per head (columns 0-127,
 // four e4m3 per column: the A operand of QK^T, so the largest operand is not
 // read from shared memory once per chunk), two 64-column S buffers, and the
 // 256-column O half. Per 64-entry chunk of the index list:
-//   gather   four warps copy this CTA's 32 of the chunk's 64 kv rows (576 B
-//            each; a whole warp per row, 16-byte cp.async, indices loaded one
-//            chunk ahead) into a K-major tile: four 128-byte swizzled regions
-//            plus one 64-byte swizzled region for the last 64 columns (invalid
-//            entries become zero rows and are masked), then five bulk copies
-//            put the same rows at the same offsets of the peer's tile; four
-//            stages;
+//   gather   four warps copy the 64 kv rows (576 B each; a whole warp per
+//            row, 16-byte cp.async, indices loaded one chunk ahead) into a
+//            K-major tile: four 128-byte swizzled regions plus one 64-byte
+//            swizzled region for the last 64 columns; invalid entries become
+//            zero rows (zero-filling copies, and masked); four stages. Each
+//            gather thread hangs its copies on the stage's full barrier
+//            (an arrival once they land) and goes on to the next chunk, so
+//            the gather runs up to four chunks ahead and a chunk is ready
+//            the moment its rows have landed;
 //   S = Q K^T  tcgen05 e4m3, M=128, N=64: 16 MMAs with A = Q's nope part in
 //            TMEM, 2 with A = its rope part in shared memory;
 //   P        one thread per head row: online softmax with a lazy reference 4
@@ -69,9 +68,8 @@ constexpr uint32_t kIdescQK = idesc_f32(128, 64);
 constexpr uint32_t kIdescPV = idesc_f32(128, 256) | (1u << 16);   // B MN-major
 
 constexpr int kMlaThreads = 288;   // MMA, 4 gather, 4 softmax warps
-constexpr uint32_t kHalfBytes = 4 * 4096 + 2048;   // one CTA's 32 rows of a chunk tile
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
+__global__ void __launch_bounds__(kMlaThreads, 1)
 mla_prefill_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_constant__ CUtensorMap tm_q64,
                    const uint8_t* __restrict__ kv, const int32_t* __restrict__ indices,
                    const int32_t* __restrict__ topk_length, const float* __restrict__ sink,
@@ -83,9 +81,6 @@ mla_prefill_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_con
   uint8_t* smem = align1024(smem_raw);
   __shared__ uint64_t bar_q, bar_qt, bar_kf[kStagesM], bar_ke[kStagesM], bar_sf[2], bar_pf[2],
       bar_pv, bar_done, bar_drain;
-  // bar_pfree[s] phase k: the peer's stage s is free for its (k+1)-th chunk,
-  // i.e. this CTA may put its rows there (arrivals come from the peer)
-  __shared__ uint64_t bar_pfree[kStagesM];
   __shared__ uint32_t tmem_base_s;
   __shared__ int abort_s;
 
@@ -101,9 +96,7 @@ mla_prefill_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_con
     mbar_init(&bar_q, 1);
     mbar_init(&bar_qt, 4);
     mbar_init(&bar_drain, 1);
-    for (int s = 0; s < kStagesM; ++s) {
-      mbar_init(&bar_kf[s], 1); mbar_init(&bar_ke[s], 1); mbar_init(&bar_pfree[s], 1);
-    }
+    for (int s = 0; s < kStagesM; ++s) { mbar_init(&bar_kf[s], 128); mbar_init(&bar_ke[s], 1); }
     for (int s = 0; s < 2; ++s) { mbar_init(&bar_sf[s], 1); mbar_init(&bar_pf[s], 4); }
     mbar_init(&bar_pv, 1);
     mbar_init(&bar_done, 1);
@@ -111,11 +104,9 @@ mla_prefill_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_con
   }
   if (warp == 0) { tmem_alloc(&tmem_base_s, 512); tmem_relinquish(); }
   __syncthreads();
-  cluster_sync();  // both CTAs' barriers exist before either touches the other's
   pdl_trigger();   // after this block's tensor-memory allocation
   tc_fence_after();
   const uint32_t tmem = tmem_base_s;
-  const uint32_t peer = uint32_t(hf ^ 1);
 
   if (warp == 0) {
     // ---------------- Q (one TMA batch), then MMA issue (whole warp, elected lane)
@@ -133,6 +124,9 @@ mla_prefill_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_con
         auto issue_s = [&](int j) -> bool {
           const int s = j % kStagesM, sb = j & 1;
           if (!mbar_wait_warp(&bar_kf[s], (j / kStagesM) & 1, err, &abort_s)) return false;
+          // the rows landed through the generic proxy (cp.async); the MMAs
+          // read them through the async proxy
+          fence_async_shared();
           tc_fence_after();
           const uint32_t sk = smem_addr(smem + kKOff + s * kKStage);
           const uint32_t d = tmem + kTS + 64 * sb;
@@ -175,76 +169,41 @@ mla_prefill_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_con
       if (lane == 0) mbar_wait(&bar_q, 0, err);
     }
   } else if (warp <= 4) {
-    // ---------------- gather warps: copy this CTA's half of chunk j, then
-    // publish chunk j-1 once it has landed (here and, by bulk copy, at the peer)
-    // Gather: warp pw copies rows 32*hf + 8*pw .. +7 of the chunk, one row at a
-    // time with all 32 lanes (576 bytes = 36 chunks of 16 bytes), so every
-    // cp.async instruction reads contiguous bytes of one kv row. Every
-    // iteration runs even after a timeout (the waits are bounded and their
-    // results unused): each chunk's copies and arrivals then still happen, so
-    // both CTAs' barriers complete and the exit handshake below stays short.
+    // ---------------- gather warps: copy chunk j and move on
+    // Warp pw copies rows 16*pw .. 16*pw+15 of the chunk, one row at a time
+    // with all 32 lanes (576 bytes = 36 chunks of 16 bytes), so every cp.async
+    // instruction reads contiguous bytes of one kv row; then each thread
+    // arrives on the chunk's full barrier once its copies have landed.
     const int pt = tid - 32, pw = pt >> 5;
-    const int row0 = 32 * hf + 8 * pw;
-    // lanes 0..7 hold the kv index of row row0 + lane, loaded one chunk ahead
+    // lanes 0..15 hold the kv index of row 16*pw + lane, loaded one chunk ahead
     int idx_next = -1;
-    if (lane < 8 && row0 + lane < len)
-      asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(idx_next) : "l"(idx_row + row0 + lane));
-    for (int j = 0; j <= nch; ++j) {
-      if (j < nch) {
-        const int s = j % kStagesM;
-        const uint32_t ph = (j / kStagesM) & 1;
-        int my_idx = idx_next;
-        const int key_n = (j + 1) * kChunkKeys + row0 + lane;
-        idx_next = -1;
-        if (lane < 8 && key_n < len)
-          asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(idx_next) : "l"(idx_row + key_n));
-        if (lane < 8 && my_idx >= S_kv) { atomicOr(err, MSA_DEVERR_DATA); my_idx = -1; }
-        mbar_wait_ab(&bar_ke[s], ph ^ 1, err, &abort_s);       // PV(j-4) done here
-        // this stage may now receive the peer's rows; and once the peer's
-        // stage s is free, this CTA's copy of chunk j-4 out of stage s has
-        // landed there, so the stage may be overwritten
-        if (pt == 0) mbar_arrive_remote(peer_smem(&bar_pfree[s], peer));
-        mbar_wait_ab(&bar_pfree[s], ph, err, &abort_s);
-        uint8_t* stage = smem + kKOff + s * kKStage;
+    if (lane < 16 && pw * 16 + lane < len)
+      asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(idx_next) : "l"(idx_row + pw * 16 + lane));
+    for (int j = 0; j < nch; ++j) {
+      const int s = j % kStagesM;
+      int my_idx = idx_next;
+      const int key_n = (j + 1) * kChunkKeys + pw * 16 + lane;
+      idx_next = -1;
+      if (lane < 16 && key_n < len)
+        asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(idx_next) : "l"(idx_row + key_n));
+      if (lane < 16 && my_idx >= S_kv) { atomicOr(err, MSA_DEVERR_DATA); my_idx = -1; }
+      // PV(j-4) done: the stage is free (the result is unused: after a
+      // timeout the loop still runs, so every thread's arrivals happen)
+      mbar_wait_ab(&bar_ke[s], ((j / kStagesM) & 1) ^ 1, err, &abort_s);
+      uint8_t* stage = smem + kKOff + s * kKStage;
 #pragma unroll 4
-        for (int rr = 0; rr < 8; ++rr) {
-          const int r = row0 + rr;
-          const int idx = __shfl_sync(0xffffffffu, my_idx, rr);
-          const uint8_t* src = kv + size_t(idx < 0 ? 0 : idx) * kDqk;
-          {
-            const int c = lane;                                  // chunks 0..31: SW128 regions
-            uint8_t* dst = stage + (c >> 3) * 8192 + swz_offset(r, c & 7, 128);
-            if (idx >= 0) cp_async16(dst, src + c * 16);
-            else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
-          }
-          if (lane < 4) {                                        // chunks 32..35: SW64 tail
-            uint8_t* dst = stage + kKTail + swz_offset(r, lane, 64);
-            if (idx >= 0) cp_async16(dst, src + (32 + lane) * 16);
-            else *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
-          }
-        }
-        cp_async_commit();
+      for (int rr = 0; rr < 16; ++rr) {
+        const int r = pw * 16 + rr;
+        const int idx = __shfl_sync(0xffffffffu, my_idx, rr);
+        const uint8_t* src = kv + size_t(idx < 0 ? 0 : idx) * kDqk;
+        cp_async16_zfill(stage + (lane >> 3) * 8192 + swz_offset(r, lane & 7, 128), src + lane * 16,
+                         idx >= 0);                          // chunks 0..31: SW128 regions
+        if (lane < 4)                                        // chunks 32..35: SW64 tail
+          cp_async16_zfill(stage + kKTail + swz_offset(r, lane, 64), src + (32 + lane) * 16, idx >= 0);
       }
-      if (j >= 1) {
-        const int sp = (j - 1) % kStagesM;
-        if (j < nch) cp_async_wait<1>(); else cp_async_wait<0>();
-        fence_async_shared();
-        asm volatile("bar.sync 2, 128;" ::: "memory");        // this CTA's half has landed
-        if (pt == 0) {
-          // the same 32 rows into the peer's stage (its stage is free: waited
-          // above before this chunk was gathered), completing on its barrier
-          uint8_t* stage = smem + kKOff + sp * kKStage;
-          const uint32_t pstage = peer_smem(stage, peer);
-          const uint32_t pbar = peer_smem(&bar_kf[sp], peer);
-#pragma unroll
-          for (int rg = 0; rg < 4; ++rg)
-            bulk_copy_to_peer(pstage + rg * 8192 + hf * 4096, stage + rg * 8192 + hf * 4096, 4096, pbar);
-          bulk_copy_to_peer(pstage + kKTail + hf * 2048, stage + kKTail + hf * 2048, 2048, pbar);
-          // own half landed; the chunk is complete when the peer's half lands too
-          mbar_arrive_expect_tx(&bar_kf[sp], kHalfBytes);
-        }
-      }
+      cp_async_arrive(&bar_kf[s]);
     }
+    cp_async_wait_all();        // nothing of this thread is in flight at the exit
   } else {
     // ---------------- softmax (warps 5-8): thread = head row (TMEM lane)
     const int q4 = warp & 3;
@@ -385,14 +344,6 @@ mla_prefill_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_con
   }
   tc_fence_before();
   __syncthreads();
-  // Exit handshake of the pair: after the first cluster barrier neither CTA
-  // issues another copy or remote arrival; each then waits (bounded; at once
-  // in the normal path, where the MMA warp already consumed every chunk) for
-  // the copies that came into its stages, and after the second barrier no
-  // copy reads or writes either CTA's shared memory any more.
-  cluster_sync();
-  if (tid == 32) mbar_drain_ring(bar_kf, kStagesM, nch, err);
-  cluster_sync();
   if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
