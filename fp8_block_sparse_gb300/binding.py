@@ -88,7 +88,8 @@ def _check(status: int) -> None:
 
 
 def _ptr(t: Optional[torch.Tensor]):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    # a plain int: ctypes turns it into the void* the signature declares
+    return None if t is None else t.data_ptr()
 
 
 def _scale(s: Optional[float]):
@@ -105,10 +106,15 @@ def _device(*tensors) -> torch.device:
     return next(iter(devs))
 
 
+_NULL_CTX = contextlib.nullcontext()
+
+
 def _on(dev: torch.device):
     """Makes `dev` the current device for the call (the library launches on
     the current device, and looks up per-device state there)."""
-    return torch.cuda.device(dev) if dev.type == "cuda" else contextlib.nullcontext()
+    if dev.type != "cuda" or dev.index is None or dev.index == torch.cuda.current_device():
+        return _NULL_CTX
+    return torch.cuda.device(dev)
 
 
 def _stream(stream: Optional[torch.cuda.Stream], dev: Optional[torch.device] = None):
@@ -240,18 +246,22 @@ def quant_fp8_multi(items, stream=None):
         if x.stride(-1) != 1:
             raise MsaError(1, "x must have a contiguous last dimension")
         cols = x.shape[-1]
-        rows = x.numel() // cols if cols else 0
-        x2 = x.reshape(rows, cols) if x.dim() != 2 else x
+        n = x.numel()
+        rows = n // cols if cols else 0
+        if x.is_contiguous():                  # rows of `cols` elements, back to back
+            x2, xstride = x, cols
+        else:
+            x2 = x.reshape(rows, cols) if x.dim() != 2 else x
+            xstride = x2.stride(0) if rows else cols
         if out is None:
             out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
-        _dev(out, "out", torch.uint8)
-        if out.numel() != x.numel():
-            raise MsaError(1, f"out must hold {x.numel()} elements, got {out.numel()}")
-        o2 = out.view(rows, cols)
+        else:
+            _dev(out, "out", torch.uint8)
+            if out.numel() != n:
+                raise MsaError(1, f"out must hold {n} elements, got {out.numel()}")
         sc = _scale(scale)
-        keep.append((x2, o2, sc))
-        descs[i] = _QuantTensor(x2.data_ptr(), rows, cols, x2.stride(0) if rows else cols,
-                                o2.data_ptr(), o2.stride(0) if rows else cols, sc)
+        keep.append((x2, sc))
+        descs[i] = _QuantTensor(x2.data_ptr(), rows, cols, xstride, out.data_ptr(), cols, sc)
         outs.append(out)
         tensors += [x, out]
     dev = _device(*tensors)

@@ -476,16 +476,19 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 // the workspace; decode_combine_kernel merges the chunks and applies the sink.
 constexpr int kDecChunk = 32;
 constexpr int kDecKStages = 3;
-constexpr int kDecVStages = 2;
+// Three V stages: V(j) may only be loaded once PV(j - stages) has read its
+// stage, so the V ring depth times a page's HBM latency sets the pace of a
+// CTA (with two stages the MMA warp waited ~1k cycles per block for V).
+constexpr int kDecVStages = 3;
 constexpr int kDecMaxList = 1024;   // union entries kept (<= 16 index heads x 64)
 constexpr int kDKOff = 0;           // kDecKStages x 16 KB K pages (SW128)
 constexpr int kDVOff = 49152;       // kDecVStages x 16 KB V pages (SW128)
-constexpr int kDPOff = 81920;       // 2 x 2 terms x 2 KB: 16 rows x 128 keys e4m3 (SW128)
-constexpr int kDBitsOff = 81920;    // setup only: 16 bitmaps x 2048 bits (aliases P)
-constexpr int kDQOff = 94208;       // 16 rows x 128 e4m3
-constexpr int kDListOff = 96256;    // union list (int16)
-constexpr int kDMaskOff = 98304;    // per-entry row mask (uint16)
-constexpr int kDecodeSmem = 100352 + 1024;
+constexpr int kDPOff = 98304;       // 2 x 2 terms x 2 KB: 16 rows x 128 keys e4m3 (SW128)
+constexpr int kDBitsOff = 98304;    // setup only: 16 bitmaps x 2048 bits (aliases P)
+constexpr int kDQOff = 106496;      // 16 rows x 128 e4m3
+constexpr int kDListOff = 108544;   // union list (int16)
+constexpr int kDMaskOff = 110592;   // per-entry row mask (uint16)
+constexpr int kDecodeSmem = 112640 + 1024;   // two CTAs per SM
 constexpr float kDecLimit = 8.0f;   // log2 of the largest P before the reference moves
 constexpr float kDecHead = 4.0f;    // log2 of P at the key that set the reference
 constexpr uint32_t kIdescDec = idesc_f32(128, 16);
