@@ -196,7 +196,7 @@ def gqa_setup(msa, wl, name, dev, pinned=False):
 
 
 LAUNCHES_PREFILL = 1 + 3 + 3     # quant (Q and idx_q, one launch); index: plan, score, select; attn: plan, V^T, attention
-LAUNCHES_DECODE = 2 + 2 + 2      # quant x2; index: score, select; attn: decode, combine
+LAUNCHES_DECODE = 1 + 2 + 2      # quant (q and idx_q, one launch); index: score, select; attn: decode, combine
 
 
 def run_path(msa, st, q_in=None, iq_in=None):
@@ -503,23 +503,59 @@ def reference_arm(args):
 
 
 def _e2e(msa, st, args, world, dev, h2d, d2h, barrier, T):
+    """End to end through the public API with host buffers: each step copies
+    its Q and idx_q in from pinned host memory, runs the path and copies O,
+    lse and max_logit back. The copies run on two copy streams (in and out)
+    against double-buffered device inputs and outputs, so step k+1's inputs
+    arrive and step k-1's outputs leave while step k computes; the timed
+    region runs from before the first copy in to after the last copy out."""
     import torch
+    comp = torch.cuda.current_stream()
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    bufs = [{k: st[k] for k in ("q", "iq", "o", "lse", "ml")},
+            {k: torch.empty_like(st[k]) for k in ("q", "iq", "o", "lse", "ml")}]
+    outs = [{"o": st["o_host"], "lse": st["lse_host"], "ml": st["ml_host"]},
+            {k: torch.empty_like(st[k + "_host"]).pin_memory() for k in ("o", "lse", "ml")}]
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(args.steps):
-        st["q"].copy_(st["q_host"], non_blocking=True)
-        st["iq"].copy_(st["iq_host"], non_blocking=True)
-        run_path(msa, st)
-        st["o_host"].copy_(st["o"], non_blocking=True)
-        st["lse_host"].copy_(st["lse"], non_blocking=True)
-        st["ml_host"].copy_(st["ml"], non_blocking=True)
-    e1.record()
+    torch.cuda.synchronize()
+    e0.record(comp)
+    up.wait_stream(comp)
+    down.wait_stream(comp)
+
+    def copy_in(k):
+        b = k % 2
+        with torch.cuda.stream(up):
+            if k >= 2:
+                up.wait_event(ev_done[b])          # step k-2 has read buffer b's inputs
+            bufs[b]["q"].copy_(st["q_host"], non_blocking=True)
+            bufs[b]["iq"].copy_(st["iq_host"], non_blocking=True)
+            ev_in[b].record(up)
+
+    copy_in(0)
+    for k in range(args.steps):
+        b = k % 2
+        if k + 1 < args.steps:
+            copy_in(k + 1)
+        comp.wait_event(ev_in[b])
+        if k >= 2:
+            comp.wait_event(ev_out[b])             # step k-2's outputs have left buffer b
+        run_path(msa, dict(st, **bufs[b]))
+        ev_done[b].record(comp)
+        with torch.cuda.stream(down):
+            down.wait_event(ev_done[b])
+            for key in ("o", "lse", "ml"):
+                outs[b][key].copy_(bufs[b][key], non_blocking=True)
+            ev_out[b].record(down)
+    comp.wait_stream(down)
+    e1.record(comp)
     barrier()
     e2e_ms = world_max(e0.elapsed_time(e1), world, dev)
-    e2e = {"value": job_throughput(T, world, args.steps, e2e_ms), "unit": UNIT,
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
-
-    return e2e
+    return {"value": job_throughput(T, world, args.steps, e2e_ms), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "copies": "two copy streams, double-buffered device inputs and outputs"}
 
 
 def native_arm(args):
