@@ -179,15 +179,31 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       pos = ti.p0 + tl;
       own = pos >> 7;
       src = topk + (size_t(h / (Hq / Hidx)) * T + t) * topk_k;
-      int last = -1;
-      for (int k = 0; hh == 0 && k < topk_k; ++k) {            // one thread per row
-        const int id = __ldg(src + k);
-        if (id < 0) continue;                                   // -1 padding
-        if (id <= last || id > own) { atomicOr(err, MSA_DEVERR_DATA); continue; }
-        atomicOr(&sBits[id >> 5], 1u << (id & 31));
-        last = id;
-      }
       next_id = topk_k > 0 ? __ldg(src) : -1;
+    }
+  }
+  {
+    // the union of the tile pair's lists: every thread takes entries of the
+    // (token, index head) lists in turn, all loads independent of one another.
+    // A list must be strictly ascending with its -1 padding at the end (each
+    // row walks its own list in union order); an entry that breaks this, or
+    // that points past its token's own block, is left out and reported.
+    const int hpi = Hq / Hidx;
+    const int i_first = (g * G) / hpi;
+    const int n_idx = (g * G + G - 1) / hpi - i_first + 1;
+    const int per_tok = n_idx * topk_k;
+    for (int x = tid; x < n_tok * per_tok; x += kPrefillThreads) {
+      const int tl = x / per_tok, r = x - tl * per_tok;
+      const int il = r / topk_k, k = r - il * topk_k;
+      const int32_t* lst = topk + (size_t(i_first + il) * T + ti.t0 + tl) * topk_k;
+      const int id = __ldg(lst + k);
+      if (id < 0) continue;                                       // -1 padding
+      const int prev = k > 0 ? __ldg(lst + k - 1) : -1;
+      if ((k > 0 && (prev < 0 || prev >= id)) || id > ((ti.p0 + tl) >> 7)) {
+        atomicOr(err, MSA_DEVERR_DATA);
+        continue;
+      }
+      atomicOr(&sBits[id >> 5], 1u << (id & 31));
     }
   }
   __syncthreads();
@@ -485,6 +501,9 @@ constexpr int kDKOff = 0;           // kDecKStages x 16 KB K pages (SW128)
 constexpr int kDVOff = 49152;       // kDecVStages x 16 KB V pages (SW128)
 constexpr int kDPOff = 98304;       // 2 x 2 terms x 2 KB: 16 rows x 128 keys e4m3 (SW128)
 constexpr int kDBitsOff = 98304;    // setup only: 16 bitmaps x 2048 bits (aliases P)
+constexpr int kDUnionOff = 102400;  // setup only: 64 union words (aliases P)
+constexpr int kDPreOff = 102656;    // setup only: 64 popcount prefixes (aliases P)
+constexpr int kDRowMaskOff = 102912;   // setup only: 16 row masks (aliases P)
 constexpr int kDQOff = 106496;      // 16 rows x 128 e4m3
 constexpr int kDListOff = 108544;   // union list (int16)
 constexpr int kDMaskOff = 110592;   // per-entry row mask (uint16)
@@ -554,8 +573,14 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
   int16_t* sList = reinterpret_cast<int16_t*>(smem + kDListOff);
   uint16_t* sMask = reinterpret_cast<uint16_t*>(smem + kDMaskOff);
   uint32_t* sBits = reinterpret_cast<uint32_t*>(smem + kDBitsOff);
+  uint32_t* sUnion = reinterpret_cast<uint32_t*>(smem + kDUnionOff);
+  int* sPre = reinterpret_cast<int*>(smem + kDPreOff);
+  uint16_t* sRowMask = reinterpret_cast<uint16_t*>(smem + kDRowMaskOff);
   for (int x = tid; x < n_idx * 64; x += kDecThreads) sBits[x] = 0u;
+  if (tid < 16) sRowMask[tid] = 0;
   __syncthreads();
+  if (tid == 0)                                    // rows of the group fed by each index head
+    for (int r = 0; r < G; ++r) sRowMask[(g * G + r) / hpi - i_first] |= uint16_t(1u << r);
   for (int x = tid; x < n_idx * topk_k; x += kDecThreads) {
     const int il = x / topk_k;
     const int id = __ldg(topk + (size_t(i_first + il) * T + t) * topk_k + (x - il * topk_k));
@@ -564,38 +589,38 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     atomicOr(&sBits[il * 64 + (id >> 5)], 1u << (id & 31));
   }
   __syncthreads();
-  if (warp == 0) {
-    int base = 0;
-    for (int w0 = 0; w0 < 64; w0 += 32) {
-      uint32_t bits = 0;
-      for (int il = 0; il < n_idx; ++il) bits |= sBits[il * 64 + w0 + lane];
-      const int cnt = __popc(bits);
-      int incl = cnt;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-      }
-      int off = base + incl - cnt;
-      uint32_t bb = bits;
-      while (bb) {
-        const int k = __ffs(bb) - 1;
-        bb &= bb - 1;
-        const int blk = (w0 + lane) * 32 + k;
-        if (off < kDecMaxList) {
-          uint32_t m = 0;
-          for (int r = 0; r < G; ++r) {
-            const int il = (g * G + r) / hpi - i_first;
-            m |= ((sBits[il * 64 + (blk >> 5)] >> (blk & 31)) & 1u) << r;
-          }
-          sList[off] = int16_t(blk);
-          sMask[off] = uint16_t(m);
-        }
-        ++off;
-      }
-      base += __shfl_sync(0xffffffffu, incl, 31);
+  if (warp == 0) {     // union words (lane: words 2 lane, 2 lane + 1) and their popcount prefix
+    uint32_t u0 = 0, u1 = 0;
+    for (int il = 0; il < n_idx; ++il) {
+      u0 |= sBits[il * 64 + 2 * lane];
+      u1 |= sBits[il * 64 + 2 * lane + 1];
     }
-    if (lane == 0) n_union_s = min(base, kDecMaxList);
+    const int c0 = __popc(u0), c1 = __popc(u1);
+    int incl = c0 + c1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    sUnion[2 * lane] = u0;
+    sUnion[2 * lane + 1] = u1;
+    sPre[2 * lane] = incl - c0 - c1;
+    sPre[2 * lane + 1] = incl - c1;
+    if (lane == 31) n_union_s = min(incl, kDecMaxList);
+  }
+  __syncthreads();
+  // every thread places the union's blocks: ascending list and per-entry row mask
+  for (int x = tid; x < 64 * 32; x += kDecThreads) {
+    const int w = x >> 5, k = x & 31;
+    const uint32_t u = sUnion[w];
+    if (!((u >> k) & 1u)) continue;
+    const int off = sPre[w] + __popc(u & ((1u << k) - 1u));
+    if (off >= kDecMaxList) continue;
+    uint32_t m = 0;
+    for (int il = 0; il < n_idx; ++il)
+      if ((sBits[il * 64 + w] >> k) & 1u) m |= sRowMask[il];
+    sList[off] = int16_t(w * 32 + k);
+    sMask[off] = uint16_t(m);
   }
   __syncthreads();                                   // the bitmaps (over P) are dead now
   const int nU = n_union_s;
