@@ -57,9 +57,10 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU oracle sample budget")
     p.add_argument("--no-e2e", action="store_true", help="skip the end-to-end measurement")
     p.add_argument("--no-mla", action="store_true", help="skip the sparse-MLA measurement")
-    p.add_argument("--only", choices=["prefill", "decode", "mla"], default=None,
+    p.add_argument("--only", choices=["prefill", "decode", "mla", "kv_store"], default=None,
                    help="run only this part of the path, warm-up + steps times, untimed, and "
-                        "print no result line (for profiler captures)")
+                        "print no result line (for profiler captures; mla also runs the rope "
+                        "producer of its q, kv_store stores the --workload's new tokens)")
     p.add_argument("--workload", default=WORKLOAD, choices=["prefill32k", "prefill8k", "tiny"],
                    help="prefill workload of the step (the benchmark line uses prefill32k)")
     return p.parse_args()
@@ -155,6 +156,21 @@ def traffic_for(kernel_file: str, profile_name: str):
         return float(fields["dram_bytes_per_launch"])
     except (KeyError, ValueError):
         return None
+
+
+class L2Flush:
+    """Evicts the 129 MB L2 before a timed step: a 256 MB write, then a
+    256 MB read, so that the lines left in L2 are clean and the step does not
+    pay for writing the flush buffer back to HBM."""
+
+    def __init__(self, dev):
+        import torch
+        self.w = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        self.r = torch.zeros(32 << 20, dtype=torch.int64, device=dev)
+
+    def __call__(self):
+        self.w.zero_()
+        self.r.sum()
 
 
 # ----------------------------------------------------------------- workloads
@@ -309,9 +325,15 @@ def mla_measure(msa, wl, dev, steps, flush, pk, only=None):
         msa.sparse_mla_fwd(q8, kv8, idx, tl, sink, w.sm_scale, w.scales["q"], w.scales["kv"],
                            out=o, max_logits=ml, lse=ls)
 
+    cs = t(wl.rotary_table(w.cfg.S_kv, 64))
+    pos = t((np.arange(T) + w.cfg.S_kv - T).astype(np.int32))
+    rq = lambda: msa.rope_quant_fp8(q[..., :512], q[..., 512:], cs, pos, is_neox=True,
+                                    scale=w.scales["q"], out=q8)
     if only is not None:
         for _ in range(only):
             step()
+        for _ in range(only):
+            rq()
         torch.cuda.synchronize()
         msa.check_errors()
         return None
@@ -320,7 +342,7 @@ def mla_measure(msa, wl, dev, steps, flush, pk, only=None):
     torch.cuda.synchronize()
     ms, kern = [], []
     for _ in range(steps):
-        flush.zero_()
+        flush()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         step()
@@ -331,16 +353,12 @@ def mla_measure(msa, wl, dev, steps, flush, pk, only=None):
     msa.check_errors()
     # the fused producer of the same q: rotary embedding of q[..., 512:] and
     # e4m3 of nope || rope(pe), one launch per step
-    cs = t(wl.rotary_table(w.cfg.S_kv, 64))
-    pos = t((np.arange(T) + w.cfg.S_kv - T).astype(np.int32))
-    rq = lambda: msa.rope_quant_fp8(q[..., :512], q[..., 512:], cs, pos, is_neox=True,
-                                    scale=w.scales["q"], out=q8)
     for _ in range(3):
         rq()
     torch.cuda.synchronize()
     r_ms = []
     for _ in range(steps):
-        flush.zero_()
+        flush()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         rq()
@@ -363,9 +381,10 @@ def mla_measure(msa, wl, dev, steps, flush, pk, only=None):
             "peak_basis": f"{pk['source']} bf16 burst x2", "rope_quant": rope}
 
 
-def kv_store_measure(msa, w, dev, steps, flush, pk):
+def kv_store_measure(msa, w, dev, steps, flush, pk, only=None):
     """The quantised KV-cache store of a workload's new tokens (K, V and index
-    K of every query row into the paged e4m3 pools), one launch per step."""
+    K of every query row into the paged e4m3 pools), one launch per step
+    (with `only` = n: just run it n times, untimed)."""
     import numpy as np
     import torch
     c = w.cfg
@@ -384,12 +403,18 @@ def kv_store_measure(msa, w, dev, steps, flush, pk):
         msa.kv_store_fp8(pt, sl, cu, kc, vc, ic, k=k, v=v, idx_k=ik,
                          k_scale=w.scales["k"], v_scale=w.scales["v"], idx_k_scale=w.scales["idx_k"])
 
+    if only is not None:
+        for _ in range(only):
+            step()
+        torch.cuda.synchronize()
+        msa.check_errors()
+        return None
     for _ in range(3):
         step()
     torch.cuda.synchronize()
     ms = []
     for _ in range(steps):
-        flush.zero_()
+        flush()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         step()
@@ -582,6 +607,8 @@ def native_arm(args):
         n = args.warmup + args.steps
         if args.only == "mla":
             mla_measure(msa, wl, dev, 0, None, pk, only=n)
+        elif args.only == "kv_store":
+            kv_store_measure(msa, wl.make_gqa(wl.CONFIGS[args.workload]), dev, 0, None, pk, only=n)
         else:
             part = gqa_setup(msa, wl, args.workload if args.only == "prefill" else "decode", dev)
             for _ in range(n):
@@ -591,7 +618,7 @@ def native_arm(args):
         return 0
 
     st = gqa_setup(msa, wl, args.workload, dev, pinned=True)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     msa.profile_enable(True)
     for _ in range(max(3, args.warmup)):
         run_path(msa, st)
@@ -610,7 +637,7 @@ def native_arm(args):
     clocks.start()
     barrier()
     for k in range(args.steps):
-        flush.zero_()
+        flush()
         s = torch.cuda.current_stream()
         ev[k][0].record(s)
         c = cuts[k]
@@ -676,7 +703,7 @@ def native_arm(args):
         torch.cuda.synchronize()
         d_ms, d_kern = [], []
         for k in range(args.steps):
-            flush.zero_()
+            flush()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
             run_path(msa, ds)
@@ -702,7 +729,7 @@ def native_arm(args):
         torch.cuda.synchronize()
         g_ms = []
         for k in range(args.steps):
-            flush.zero_()
+            flush()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
             graph.replay()
@@ -752,7 +779,7 @@ def native_arm(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
             "config": {"workload": args.workload, "tokens": T, "Hq": 16, "Hkv": 2, "Hidx": 4, "head_dim": 128,
                        "d_idx": 128, "topk": 64, "page": 128, "parallelism": f"replicas x{world}",
-                       "l2": "flushed (256 MB write) before every timed step"},
+                       "l2": "flushed before every timed step: 256 MB write, then 256 MB read (the step starts with clean lines, so the flush's write-back is not charged to it)"},
             "roofline": roof,
             "prefill_tflops_algorithmic": flops / (total_ms / args.steps / 1e3) / 1e12,
             "breakdown_ms": {"quant": quant_ms, "index_topk": index_ms, "attention_call": attn_call_ms,
