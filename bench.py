@@ -370,7 +370,7 @@ def mla_measure(msa, wl, dev, steps, flush, pk, only=None):
     rm = statistics.mean(r_ms)
     rope = {"kernel": "rope_quant_kernel", "rows": T, "heads": H, "d_nope": 512, "d_rope": 64, "ms": rm,
             "gbs": r_bytes / (rm / 1e3) / 1e9, "frac_of_hbm": r_bytes / (rm / 1e3) / 1e9 / pk["hbm_gbs"],
-            "algorithmic_bytes": r_bytes}
+            "algorithmic_bytes": r_bytes, "traffic": traffic_for("quant.cu", "rope_quant_kernel_mla_q.md")}
     flops = float(np.sum(w.topk_length.astype(np.float64))) * H * (2 * 576 + 2 * 512)
     k = statistics.mean(kern)
     fp8_peak = 2.0 * pk["bf16_tflops"]
@@ -378,6 +378,7 @@ def mla_measure(msa, wl, dev, steps, flush, pk, only=None):
             "tokens_per_s": T / (statistics.mean(ms) / 1e3),
             "kernel": "mla_prefill_kernel", "kernel_ms": k, "tflops_algorithmic": flops / (k / 1e3) / 1e12,
             "frac_of_fp8_peak": flops / (k / 1e3) / 1e12 / fp8_peak, "algorithmic_flop": flops,
+            "traffic": traffic_for("mla.cu", "mla_prefill_kernel_mla.md"),
             "peak_basis": f"{pk['source']} bf16 burst x2", "rope_quant": rope}
 
 
@@ -429,7 +430,8 @@ def kv_store_measure(msa, w, dev, steps, flush, pk, only=None):
     del kc, vc, ic, k, v, ik
     return {"workload": c.name, "tokens": T, "kernel": "kv_store_kernel", "ms": m,
             "gbs": nbytes / (m / 1e3) / 1e9, "frac_of_hbm": nbytes / (m / 1e3) / 1e9 / pk["hbm_gbs"],
-            "algorithmic_bytes": nbytes, "peak_basis": pk["source"]}
+            "algorithmic_bytes": nbytes, "peak_basis": pk["source"],
+            "traffic": traffic_for("quant.cu", "kv_store_kernel_prefill32k.md") if c.name == "prefill32k" else None}
 
 
 # ----------------------------------------------------------------- CPU oracle
@@ -666,6 +668,21 @@ def native_arm(args):
     kern_ms = statistics.mean(attn_ms)
     msa.check_errors()
 
+    # ---- the quantiser's kernel alone (library events around its launch;
+    # the step's quantise breakdown above also holds the host time of the call)
+    qk_ms = []
+    for _ in range(args.steps):
+        flush()
+        msa.quant_fp8_multi([(st["q"], st["w"].scales["q"], st["q8"]),
+                             (st["iq"], st["w"].scales["idx_q"], st["iq8"])])
+        qk_ms.append(msa.profile_last_ms())
+    msa.check_errors()
+    q_bytes = 3.0 * (st["q"].numel() + st["iq"].numel())
+    qk = statistics.mean(qk_ms)
+    quant_kernel = {"kernel": "quant_multi_kernel", "ms": qk, "algorithmic_bytes": q_bytes,
+                    "gbs": q_bytes / (qk / 1e3) / 1e9, "frac_of_hbm": q_bytes / (qk / 1e3) / 1e9 / pk["hbm_gbs"],
+                    "traffic": traffic_for("quant.cu", "quant_multi_kernel_prefill32k.md")}
+
     T = st["w"].T
     value = job_throughput(T, world, args.steps, total_ms)
     n_keys = selected_keys(st)
@@ -675,7 +692,7 @@ def native_arm(args):
     achieved = flops / (kern_ms / 1e3) / 1e12
     roof = {"bound": "tensor", "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
             "frac": achieved / fp8_peak,
-            "traffic": traffic_for("attn.cu", "attn_prefill_kernel_prefill32k_traffic.md"),
+            "traffic": traffic_for("attn.cu", "attn_prefill_kernel_prefill32k.md"),
             "kernel": "attn_prefill_kernel",
             "peak_basis": f"{pk['source']} bf16 burst {pk['bf16_tflops']:.0f} TF/s x2 (nominal fp8/bf16 ratio)",
             "algorithmic_flop_per_launch": flops, "executed_flop_per_launch": exe,
@@ -751,7 +768,7 @@ def native_arm(args):
                   "attn_kernel": {"kernel": "attn_decode_kernel", "ms": kern_d,
                                   "gbs": kv_b / (kern_d / 1e3) / 1e9,
                                   "frac_of_hbm": kv_b / (kern_d / 1e3) / 1e9 / pk["hbm_gbs"],
-                                  "traffic": traffic_for("attn.cu", "attn_decode_kernel_decode_traffic.md")},
+                                  "traffic": traffic_for("attn.cu", "attn_decode_kernel_decode.md")},
                   "algorithmic_bytes_per_step": total_b, "kv_union_blocks": union,
                   "peak_hbm_gbs": pk["hbm_gbs"], "peak_basis": pk["source"],
                   "graph_replay": {"ms_per_step": step_ms_g, "tokens_per_s": ds["w"].T / (step_ms_g / 1e3),
@@ -784,6 +801,7 @@ def native_arm(args):
             "prefill_tflops_algorithmic": flops / (total_ms / args.steps / 1e3) / 1e12,
             "breakdown_ms": {"quant": quant_ms, "index_topk": index_ms, "attention_call": attn_call_ms,
                              "attention_kernel": kern_ms},
+            "quant_kernel": quant_kernel,
             "decode": decode,
             "mla": mla,
             "kv_store": kv_store,

@@ -272,7 +272,9 @@ msa_status msa_quant_fp8_multi(const msa_quant_tensor* tensors, int n, msa_dtype
     q.s_inv[q.n] = s_inv[i];
     ++q.n;
   }
+  if (q.n > 0) profile_mark(st, 0);
   cudaError_t e = launch_quant_multi(q, x_dtype == MSA_BF16, st);
+  if (q.n > 0) profile_mark(st, 1);
   if (e != cudaSuccess) return cuda_fail(e, fn);
   for (int i = 0; i < n; ++i) {            // the rest, one launch each
     const msa_quant_tensor& t = tensors[i];
