@@ -677,6 +677,15 @@ def native_arm(args):
                              (st["iq"], st["w"].scales["idx_q"], st["iq8"])])
         qk_ms.append(msa.profile_last_ms())
     msa.check_errors()
+    # ---- the index step's kernels alone (scoring through selection)
+    ik_ms = []
+    for _ in range(args.steps):
+        flush()
+        w = st["w"]
+        msa.index_topk(st["iq8"], st["ik8"], st["pt"], st["sl"], st["cu"], w.cfg.topk, w.max_q_len,
+                       out=st["ids"], workspace=st["ws_idx"])
+        ik_ms.append(msa.profile_last_ms())
+    msa.check_errors()
     q_bytes = 3.0 * (st["q"].numel() + st["iq"].numel())
     qk = statistics.mean(qk_ms)
     quant_kernel = {"kernel": "quant_multi_kernel", "ms": qk, "algorithmic_bytes": q_bytes,
@@ -802,6 +811,7 @@ def native_arm(args):
             "breakdown_ms": {"quant": quant_ms, "index_topk": index_ms, "attention_call": attn_call_ms,
                              "attention_kernel": kern_ms},
             "quant_kernel": quant_kernel,
+            "index_kernels_ms": statistics.mean(ik_ms),
             "decode": decode,
             "mla": mla,
             "kv_store": kv_store,

@@ -12,10 +12,10 @@
 // * Prefill scoring is a dense FP8 contraction, so it runs on tcgen05: a CTA
 //   holds a 128-row tile of (token, index head) queries in shared memory (one
 //   TMA load) and streams the 128-key pages of the index-K cache through a
-//   4-stage TMA ring. Each page is one M=128 x N=128 x K=D e4m3 MMA into a
+//   3-stage TMA ring. Each page is one M=128 x N=128 x K=D e4m3 MMA into a
 //   double-buffered TMEM accumulator; four epilogue warps read their rows out
 //   of TMEM and reduce the 128 columns to the block maximum. Scores of a
-//   32-block chunk are staged in shared memory and written as contiguous rows.
+//   64-block chunk are staged in shared memory and written as contiguous rows.
 // * Decode (one query token per sequence) is a stream over the index-K pages;
 //   it runs the same MMA with the roles swapped (M=128 keys of the page,
 //   N=16 query columns of which Hidx are used) so the page is the A operand
@@ -30,8 +30,8 @@
 namespace msa {
 namespace {
 
-constexpr int kChunk = 32;       // blocks scored per CTA
-constexpr int kStages = 4;       // TMA ring depth
+constexpr int kChunk = 64;       // blocks scored per CTA (64 measured 7% faster than 32 and 48)
+constexpr int kStages = 3;       // TMA ring depth (3 keeps two CTAs per SM with 64-block chunks)
 constexpr int kScorePitch = kChunk + 1;
 
 // Order-preserving map of fp32 onto uint32 (larger float -> larger key).
@@ -176,7 +176,7 @@ index_score_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
 }
 
 // ------------------------------------------------------------ decode scores
-// One CTA per (query token, 32-block chunk). A = index-K page (M = 128 keys),
+// One CTA per (query token, 64-block chunk). A = index-K page (M = 128 keys),
 // B = the token's Hidx query rows (N = 16; extra rows are ignored).
 template <int D>
 __global__ void __launch_bounds__(192, 1)
@@ -304,36 +304,11 @@ index_score_decode_kernel(const __grid_constant__ CUtensorMap tm_q,
 
 // ------------------------------------------------------------ selection
 
-// One warp per (index head, token) row. NPL = candidate slots per lane.
+// The ascending top-(kp) of the `own` candidate blocks 0..own-1 of one row,
+// plus the own block, by one warp; NPL = candidate slots per lane
+// (32 * NPL >= own), so a short row costs only the slots it needs.
 template <int NPL>
-__global__ void __launch_bounds__(256)
-topk_select_kernel(const float* __restrict__ scores, const int32_t* __restrict__ seq_lens,
-                   const int32_t* __restrict__ cu_q, int B, int T, int Hidx, int topk,
-                   int max_pages, int decode, int32_t* __restrict__ out, unsigned* err) {
-  pdl_wait();      // the scores come from the scoring kernel
-  pdl_trigger();
-  const int lane = threadIdx.x & 31;
-  const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (row >= (long long)Hidx * T) return;
-  const int i = int(row / T), t = int(row % T);
-  // with one query per sequence (decode: q_len <= 1, T == B) token t is
-  // sequence t; otherwise search the query offsets
-  const int b = (decode && T == B) ? t : find_sequence(cu_q, B, t);
-  const int qlen = cu_q[b + 1] - cu_q[b];
-  const int p = seq_lens[b] - qlen + (t - cu_q[b]);
-  int32_t* o = out + size_t(row) * topk;
-  if (p < 0 || p >= max_pages * 128) {
-    for (int j = lane; j < topk; j += 32) o[j] = -1;
-    if (lane == 0) atomicOr(err, MSA_DEVERR_DATA);
-    return;
-  }
-  const int own = p / 128;
-  if (own + 1 <= topk) {
-    for (int j = lane; j < topk; j += 32) o[j] = (j <= own) ? j : -1;
-    return;
-  }
-  const int kp = topk - 1;
-  const float* s = scores + (size_t(i) * T + t) * max_pages;
+MSA_DEV void select_row(const float* __restrict__ s, int own, int kp, int lane, int32_t* __restrict__ o) {
   uint32_t key[NPL];
 #pragma unroll
   for (int r = 0; r < NPL; ++r) {
@@ -388,6 +363,45 @@ topk_select_kernel(const float* __restrict__ scores, const int32_t* __restrict__
   if (lane == 0) o[kp] = own;
 }
 
+// One warp per (index head, token) row. NPL = candidate slots per lane for
+// the longest row (32 * NPL >= max_pages); each row takes the smallest of
+// 2, 4, 8, 16, NPL slots that holds its candidates (warp-uniform choice).
+template <int NPL>
+__global__ void __launch_bounds__(256)
+topk_select_kernel(const float* __restrict__ scores, const int32_t* __restrict__ seq_lens,
+                   const int32_t* __restrict__ cu_q, int B, int T, int Hidx, int topk,
+                   int max_pages, int decode, int32_t* __restrict__ out, unsigned* err) {
+  pdl_wait();      // the scores come from the scoring kernel
+  pdl_trigger();
+  const int lane = threadIdx.x & 31;
+  const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= (long long)Hidx * T) return;
+  const int i = int(row / T), t = int(row % T);
+  // with one query per sequence (decode: q_len <= 1, T == B) token t is
+  // sequence t; otherwise search the query offsets
+  const int b = (decode && T == B) ? t : find_sequence(cu_q, B, t);
+  const int qlen = cu_q[b + 1] - cu_q[b];
+  const int p = seq_lens[b] - qlen + (t - cu_q[b]);
+  int32_t* o = out + size_t(row) * topk;
+  if (p < 0 || p >= max_pages * 128) {
+    for (int j = lane; j < topk; j += 32) o[j] = -1;
+    if (lane == 0) atomicOr(err, MSA_DEVERR_DATA);
+    return;
+  }
+  const int own = p / 128;
+  if (own + 1 <= topk) {
+    for (int j = lane; j < topk; j += 32) o[j] = (j <= own) ? j : -1;
+    return;
+  }
+  const float* s = scores + (size_t(i) * T + t) * max_pages;
+  const int kp = topk - 1;
+  if (NPL > 2 && own <= 64) select_row<2>(s, own, kp, lane, o);
+  else if (NPL > 4 && own <= 128) select_row<4>(s, own, kp, lane, o);
+  else if (NPL > 8 && own <= 256) select_row<(NPL > 8 ? 8 : NPL)>(s, own, kp, lane, o);
+  else if (NPL > 16 && own <= 512) select_row<(NPL > 16 ? 16 : NPL)>(s, own, kp, lane, o);
+  else select_row<NPL>(s, own, kp, lane, o);
+}
+
 }  // namespace
 
 size_t index_workspace_bytes(int T, int Hidx, int max_pages) {
@@ -433,35 +447,38 @@ cudaError_t launch_index_topk(const IndexArgs& a, cudaStream_t stream, const cha
       return cudaErrorInvalidValue;
   }
   const int chunks = (a.max_pages + kChunk - 1) / kChunk;
+  cudaError_t e = cudaSuccess;
   if (decode) {
     const int smem = kStages * 16384 + 16 * 128 + 1024;
     auto kern = D == 128 ? index_score_decode_kernel<128> : index_score_decode_kernel<64>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
+    profile_mark(stream, 0);
     e = launch_pdl(kern, a.T * chunks, 192, smem, stream, tm_q, tm_k, a.page_table, a.seq_lens,
                    a.cu_q, a.B, a.T, a.Hidx, a.max_pages, a.num_pages, chunks, scores, a.err);
     if (e != cudaSuccess) return e;
   } else {
-    cudaError_t e = launch_pdl(plan_tiles_kernel, 1, 256, 0, stream, a.seq_lens, a.cu_q, a.B, toks,
-                               a.max_pages, max_tiles, tiles, n_tiles, a.err);
+    e = launch_pdl(plan_tiles_kernel, 1, 256, 0, stream, a.seq_lens, a.cu_q, a.B, toks,
+                   a.max_pages, max_tiles, tiles, n_tiles, a.err);
     if (e != cudaSuccess) return e;
     const int smem = D == 128 ? PrefillSmem<128>::kBytes : PrefillSmem<64>::kBytes;
     auto kern = D == 128 ? index_score_prefill_kernel<128> : index_score_prefill_kernel<64>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     const int n_tiles_max = (a.T + toks - 1) / toks + a.B;
+    profile_mark(stream, 0);
     e = launch_pdl(kern, n_tiles_max * chunks, 192, smem, stream, tm_q, tm_k, a.page_table, tiles,
                    n_tiles, a.T, a.Hidx, toks, a.max_pages, a.num_pages, chunks, scores, a.err);
     if (e != cudaSuccess) return e;
   }
   const long long rows = (long long)a.Hidx * a.T;
   const int grid = int((rows + 7) / 8);
-  if (a.max_pages <= 256)
-    return launch_pdl(topk_select_kernel<8>, grid, 256, 0, stream, scores, a.seq_lens, a.cu_q, a.B, a.T, a.Hidx, a.topk, a.max_pages, int(decode), a.topk_indices, a.err);
-  else if (a.max_pages <= 512)
-    return launch_pdl(topk_select_kernel<16>, grid, 256, 0, stream, scores, a.seq_lens, a.cu_q, a.B, a.T, a.Hidx, a.topk, a.max_pages, int(decode), a.topk_indices, a.err);
-  else
-    return launch_pdl(topk_select_kernel<64>, grid, 256, 0, stream, scores, a.seq_lens, a.cu_q, a.B, a.T, a.Hidx, a.topk, a.max_pages, int(decode), a.topk_indices, a.err);
+  auto sel = a.max_pages <= 256 ? topk_select_kernel<8>
+            : a.max_pages <= 512 ? topk_select_kernel<16> : topk_select_kernel<64>;
+  e = launch_pdl(sel, grid, 256, 0, stream, scores, a.seq_lens, a.cu_q, a.B, a.T, a.Hidx, a.topk,
+                 a.max_pages, int(decode), a.topk_indices, a.err);
+  profile_mark(stream, 1);
+  return e;
 }
 
 }  // namespace msa

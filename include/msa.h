@@ -94,9 +94,10 @@ const char* msa_last_error_string(void);
  * every msa_sparse_attn_fwd and msa_sparse_mla_fwd call records a pair of
  * CUDA events on its stream around its main attention kernel (the prefill,
  * decode or MLA kernel; not the small planning, conversion or combine
- * kernels), and every msa_quant_fp8_multi call around its one-launch
- * kernel (when some tensor went to it). msa_profile_last_ms waits for the
- * most recent stop event and
+ * kernels), every msa_index_topk / msa_index_topk_noalloc call from its
+ * scoring kernel to the end of its selection kernel, and every
+ * msa_quant_fp8_multi call around its one-launch kernel (when some tensor
+ * went to it). msa_profile_last_ms waits for the most recent stop event and
  * returns the elapsed milliseconds. Disabled by default; the events belong to
  * the library (one pair per device). Do not enable during graph capture.
  */
