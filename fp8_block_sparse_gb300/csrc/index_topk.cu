@@ -53,8 +53,10 @@ struct PrefillSmem {
   static constexpr int kBytes = kScore + 128 * kScorePitch * 4 + 1024;   // + alignment slack
 };
 
+// 128 registers at most: two CTAs per SM put up to four of their warps on
+// one sub-partition, whose register file holds 4 x 32 x 128.
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __maxnreg__(128)
 index_score_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                            const __grid_constant__ CUtensorMap tm_k,
                            const int32_t* __restrict__ page_table,
@@ -147,14 +149,23 @@ index_score_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
       const int buf = j & 1;
       if (!mbar_wait_warp(&bar_tfull[buf], (j >> 1) & 1, err, &abort_s)) break;   // uniform
       tc_fence_after();
-      float m = -INFINITY;
+      // the row's 128 scores in two TMEM round trips of 64 (128 live values
+      // would cost the second CTA per SM its registers), reduced by 3-input
+      // maxima in four independent chains (every score is finite)
+      float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 128; c += 32) {
-        uint32_t v[32];
-        tmem_ld32(tmem_addr(tmem + buf * 128, (warp & 3) * 32, c), v);
+      for (int c = 0; c < 128; c += 64) {
+        uint32_t v[64];
+        tmem_ld64(tmem_addr(tmem + buf * 128, (warp & 3) * 32, c), v);
 #pragma unroll
-        for (int x = 0; x < 32; ++x) m = fmaxf(m, __uint_as_float(v[x]));
+        for (int x = 0; x < 64; x += 8) {
+          a0 = fmax3(a0, __uint_as_float(v[x]), __uint_as_float(v[x + 1]));
+          a1 = fmax3(a1, __uint_as_float(v[x + 2]), __uint_as_float(v[x + 3]));
+          a2 = fmax3(a2, __uint_as_float(v[x + 4]), __uint_as_float(v[x + 5]));
+          a3 = fmax3(a3, __uint_as_float(v[x + 6]), __uint_as_float(v[x + 7]));
+        }
       }
+      const float m = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_tempty[buf]);
