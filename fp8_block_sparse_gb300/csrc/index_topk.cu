@@ -172,13 +172,17 @@ index_score_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
       sScore[row * kScorePitch + j] = m;
     }
     asm volatile("bar.sync 1, 128;" ::: "memory");
-    // rows -> (token, head); each row writes its nblk scores contiguously
-    const int et = tid - 64;
-    for (int x = et; x < 128 * nblk; x += 128) {
-      const int r = x / nblk, jj = x - r * nblk;
-      const int tok = ti.t0 + r / Hidx, head = r % Hidx;
-      if (r / Hidx < n_tok)
-        scores[(size_t(head) * T + tok) * max_pages + c0 + jj] = sScore[r * kScorePitch + jj];
+    // rows -> (token, head): warp e takes rows e, e+4, ..., its lanes write
+    // a row's nblk scores as contiguous words (Hidx is a power of two, so
+    // the row's token and head come from a shift and a mask; a division per
+    // element made this store a quarter of the CTA's time)
+    const int hshift = __ffs(Hidx) - 1;
+    for (int r = warp - 2; r < 128; r += 4) {
+      const int tl = r >> hshift;
+      if (tl >= n_tok) break;                                 // rows are token-major
+      float* dst = scores + (size_t(r & (Hidx - 1)) * T + ti.t0 + tl) * max_pages + c0;
+      const float* src = sScore + r * kScorePitch;
+      for (int jj = lane; jj < nblk; jj += 32) dst[jj] = src[jj];
     }
   }
   tc_fence_before();
