@@ -582,7 +582,25 @@ def _e2e(msa, st, args, world, dev, h2d, d2h, barrier, T):
     e2e_ms = world_max(e0.elapsed_time(e1), world, dev)
     return {"value": job_throughput(T, world, args.steps, e2e_ms), "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "copies": "two copy streams, double-buffered device inputs and outputs"}
+            "copies": "two copy streams, double-buffered device inputs and outputs",
+            "host_copy_gbs": _host_copy_rates(st)}
+
+
+def _host_copy_rates(st):
+    """This box's pinned-memory copy rates on the step's own buffers (one
+    H2D of Q and one D2H of O, timed alone): the context of the e2e number,
+    which such rates bound from below."""
+    import torch
+    a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    torch.cuda.synchronize()
+    a.record()
+    st["q"].copy_(st["q_host"], non_blocking=True)
+    b.record()
+    st["o_host"].copy_(st["o"], non_blocking=True)
+    c.record()
+    torch.cuda.synchronize()
+    return {"h2d": st["q_host"].numel() * 2 / (a.elapsed_time(b) / 1e3) / 1e9,
+            "d2h": st["o_host"].numel() * 2 / (b.elapsed_time(c) / 1e3) / 1e9}
 
 
 def native_arm(args):

@@ -153,6 +153,17 @@ MSA_DEV void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int x
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(x), "r"(y), "r"(z)
       : "memory");
 }
+// Tiled TMA store of one box from shared memory (bulk-group completion):
+// bulk_commit() closes the group, bulk_wait_read() waits until the copies
+// have read their shared-memory source (it may then be reused or released).
+MSA_DEV void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];"
+      ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(src)), "r"(x), "r"(y)
+      : "memory");
+}
+MSA_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+MSA_DEV void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 // Plain bulk copy global -> shared (both 16-byte aligned, size a multiple of 16).
 MSA_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(

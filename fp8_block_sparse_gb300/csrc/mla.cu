@@ -36,6 +36,8 @@
 //   O += P V tcgen05 e4m3, M=128, N=256, K=64 per term: A = the P terms in
 //            TMEM, B = this CTA's 256 V columns read straight out of the
 //            gathered tile as an MN-major operand (no conversion pass).
+// Epilogue: O / Z in bf16 is staged in the freed K stages (128-byte swizzled
+// rows) and leaves as four TMA stores of 64 x 128 boxes.
 // Two e4m3 terms carry P to about 2^-8 of its value: emulated on the CPU over
 // full-size queries they cost no more than f16 P (the bf16 rounding of O
 // dominates both), while a single e4m3 term costs ~2% relative error.
@@ -71,7 +73,7 @@ constexpr int kMlaThreads = 288;   // MMA, 4 gather, 4 softmax warps
 
 __global__ void __launch_bounds__(kMlaThreads, 1)
 mla_prefill_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_constant__ CUtensorMap tm_q64,
-                   const uint8_t* __restrict__ kv, const int32_t* __restrict__ indices,
+                   const __grid_constant__ CUtensorMap tm_o, const uint8_t* __restrict__ kv, const int32_t* __restrict__ indices,
                    const int32_t* __restrict__ topk_length, const float* __restrict__ sink,
                    float qk_scale2, float sink_scale2, float v_scale, int T, int S_kv, int topk,
                    uint16_t* __restrict__ out, float* __restrict__ max_logits,
@@ -317,7 +319,12 @@ mla_prefill_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_con
     const float ls = (sig2 == -INFINITY) ? 0.f : exp2f(sig2 - M);
     const float Z = l * a + ls;
     const float so = (Z > 0.f && nch > 0) ? (a / Z) * v_scale : 0.f;
-    uint16_t* orow = out + (size_t(t) * 128 + row) * kDv + hf * 256;
+    // O / Z in bf16 through shared memory (the K stages, free once PV of
+    // the last chunk is done) and four TMA stores of 64-column boxes, so
+    // the 64 KB leave as whole lines instead of 16-byte pieces of 32 rows
+    // per store instruction. Box b holds columns 64b..64b+63 of this
+    // CTA's half, a 128-byte row per head, 16-byte chunks swizzled by row.
+    uint8_t* stg = smem + kKOff;
 #pragma unroll 2
     for (int c = 0; c < 256; c += 32) {
       uint32_t v[32];
@@ -327,6 +334,7 @@ mla_prefill_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_con
 #pragma unroll
         for (int e = 0; e < 32; ++e) v[e] = 0u;
       }
+      uint8_t* rowp = stg + (c >> 6) * 16384 + row * 128;
 #pragma unroll
       for (int e = 0; e < 32; e += 8) {
         uint4 o;
@@ -334,8 +342,17 @@ mla_prefill_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_con
         o.y = pack_bf16x2(__uint_as_float(v[e + 2]) * so, __uint_as_float(v[e + 3]) * so);
         o.z = pack_bf16x2(__uint_as_float(v[e + 4]) * so, __uint_as_float(v[e + 5]) * so);
         o.w = pack_bf16x2(__uint_as_float(v[e + 6]) * so, __uint_as_float(v[e + 7]) * so);
-        *reinterpret_cast<uint4*>(orow + c + e) = o;
+        const uint32_t chunk = uint32_t(((c & 63) + e) >> 3);
+        *reinterpret_cast<uint4*>(rowp + ((chunk ^ uint32_t(row & 7)) << 4)) = o;
       }
+    }
+    fence_async_shared();
+    asm volatile("bar.sync 1, 128;" ::: "memory");            // the four softmax warps
+    if (tid == 160) {
+#pragma unroll
+      for (int b = 0; b < 4; ++b) tma_store_2d(&tm_o, stg + b * 16384, hf * 256 + 64 * b, t * 128);
+      bulk_commit();
+      bulk_wait_read();            // the staging must stay until the copies have read it
     }
     if (hf == 0) {
       max_logits[size_t(t) * 128 + row] = m_true * kLn2;
@@ -350,7 +367,7 @@ mla_prefill_kernel(const __grid_constant__ CUtensorMap tm_q128, const __grid_con
 }  // namespace
 
 cudaError_t launch_sparse_mla(const MlaArgs& a, cudaStream_t stream, const char** why) {
-  CUtensorMap tm_q128, tm_q64;
+  CUtensorMap tm_q128, tm_q64, tm_o;
   const uint64_t dims[2] = {uint64_t(kDqk), uint64_t(a.T) * 128};
   const uint64_t strides[1] = {uint64_t(kDqk)};
   const uint32_t box128[2] = {128, 128}, box64[2] = {64, 128};
@@ -359,10 +376,18 @@ cudaError_t launch_sparse_mla(const MlaArgs& a, cudaStream_t stream, const char*
       !encode_tensor_map(&tm_q64, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, a.q, dims, strides, box64,
                          CU_TENSOR_MAP_SWIZZLE_64B, why))
     return cudaErrorInvalidValue;
+  {
+    const uint64_t odims[2] = {uint64_t(kDv), uint64_t(a.T) * 128};
+    const uint64_t ostrides[1] = {uint64_t(kDv) * 2};
+    const uint32_t obox[2] = {64, 128};
+    if (!encode_tensor_map(&tm_o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.out, odims, ostrides, obox,
+                           CU_TENSOR_MAP_SWIZZLE_128B, why))
+      return cudaErrorInvalidValue;
+  }
   cudaError_t e = cudaFuncSetAttribute(mla_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMlaSmem);
   if (e != cudaSuccess) return e;
   profile_mark(stream, 0);
-  e = launch_pdl(mla_prefill_kernel, a.T * 2, kMlaThreads, kMlaSmem, stream, tm_q128, tm_q64, a.kv,
+  e = launch_pdl(mla_prefill_kernel, a.T * 2, kMlaThreads, kMlaSmem, stream, tm_q128, tm_q64, tm_o, a.kv,
                  a.indices, a.topk_length, a.sink, a.c_qk * kLog2e, a.c_sink * kLog2e, a.v_scale,
                  a.T, a.S_kv, a.topk, a.out, a.max_logits, a.lse, a.err);
   profile_mark(stream, 1);
