@@ -395,10 +395,13 @@ topk_select_kernel(const float* __restrict__ scores, const int32_t* __restrict__
   // with one query per sequence (decode: q_len <= 1, T == B) token t is
   // sequence t; otherwise search the query offsets
   const int b = (decode && T == B) ? t : find_sequence(cu_q, B, t);
-  const int qlen = cu_q[b + 1] - cu_q[b];
-  const int p = seq_lens[b] - qlen + (t - cu_q[b]);
+  const int qlen = cu_q[b + 1] - cu_q[b], L = seq_lens[b];
+  const int p = L - qlen + (t - cu_q[b]);
   int32_t* o = out + size_t(row) * topk;
-  if (p < 0 || p >= max_pages * 128) {
+  // a token outside every sequence, or of a sequence that does not fit its
+  // page-table row (the tile plan gives it no scores): a -1 row and a data error
+  if (t >= cu_q[b + 1] || qlen < 0 || L < qlen || L > max_pages * 128 || p < 0 ||
+      p >= max_pages * 128) {
     for (int j = lane; j < topk; j += 32) o[j] = -1;
     if (lane == 0) atomicOr(err, MSA_DEVERR_DATA);
     return;

@@ -283,6 +283,10 @@ size_t msa_index_topk_workspace_size(int T, int Hidx, int max_pages);
  *               bytes, 256-byte aligned; contents on entry are ignored.
  * Supported: D in {64, 128}; 1 <= topk <= 64; Hidx a power of two <= 16;
  * max_pages <= 2048.
+ * Data errors (a sequence whose seq_len exceeds max_pages * 128 or is below
+ * its query count, a row past cu_q[B], a page id outside [0, num_pages)):
+ *   MSA_ERR_DATA is recorded for msa_check_errors(); the rows of tokens that
+ *   belong to no valid sequence are written as -1.
  */
 msa_status msa_index_topk(const uint8_t* idx_q, const uint8_t* idx_k_cache,
                           const int32_t* page_table, const int32_t* seq_lens,

@@ -125,3 +125,32 @@ def test_bad_page_id_is_reported_not_trapped(msa):
         msa.check_errors()
     assert e.value.status == 6
     msa.check_errors()      # the word was cleared
+
+
+def test_rows_of_a_rejected_sequence_are_minus_one(msa):
+    # the middle sequence claims more tokens than its page-table row holds:
+    # its rows are -1, the error is reported, the other sequences are exact
+    cfg = wl.GQAConfig("varlen", 3, (700, 1500, 2100), 0, 16, 2, 4, 128, 128, 8, "channel",
+                       pool_factor=1.2, seed=11)
+    w = wl.make_gqa(cfg)
+    q_lens = np.array([700, 300, 257], np.int32)
+    w.cu_q = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
+    T = int(w.cu_q[-1])
+    w.q, w.idx_q = w.q[:T], w.idx_q[:T]
+    ik = oq.quantize(w.idx_k_pool, w.scales["idx_k"])
+    good = np.r_[np.arange(0, 700), np.arange(1000, T)]
+    apply_no_tie(w, ik, cfg.topk, good)
+    iq = oq.quantize(w.idx_q, w.scales["idx_q"])
+    bad = w.seq_lens.copy()
+    bad[1] = w.page_table.shape[1] * 128 + 1
+    ids = msa.index_topk(dev(iq), dev(ik), dev(w.page_table), dev(bad), dev(w.cu_q), cfg.topk,
+                         w.max_q_len)
+    with pytest.raises(msa.MsaError) as e:
+        msa.check_errors()
+    assert e.value.status == 6
+    got = ids.cpu().numpy()
+    assert (got[:, 700:1000] == -1).all()
+    ref, gaps = oi.index_topk(iq, ik, w.page_table, w.seq_lens, w.cu_q, cfg.topk, tokens=good)
+    bound = no_tie.row_bounds(iq, ik, w.page_table, w.seq_lens, w.cu_q, good)
+    _, pos = oi.query_positions(w.seq_lens, w.cu_q)
+    assert check_topk_rows(got[:, good], ref, gaps, bound, pos[good] // 128, cfg.topk) == 0
