@@ -517,6 +517,15 @@ struct DecodePartial {   // per (token, kv head, chunk, row)
   float m, l, m_true, pad;
 };
 
+// The most index heads one kv group's query heads read (a group of G heads
+// starting at head g*G spans index heads (g*G)/hpi .. (g*G+G-1)/hpi).
+inline int dec_group_index_heads(int Hq, int Hkv, int Hidx) {
+  const int G = Hq / Hkv, hpi = Hq / Hidx;
+  int n = 1;
+  for (int g = 0; g < Hkv; ++g) n = max(n, (g * G + G - 1) / hpi - (g * G) / hpi + 1);
+  return n;
+}
+
 __host__ __device__ inline int dec_max_chunks(int n_idx_per_group, int topk, int max_pages) {
   const int cap = min(max_pages, n_idx_per_group * topk);
   return max(1, (cap + kDecChunk - 1) / kDecChunk);
@@ -937,8 +946,8 @@ decode_combine_kernel(const float* __restrict__ part_o, const DecodePartial* __r
 }
 
 cudaError_t launch_decode(const AttnArgs& a, cudaStream_t stream, const char** why) {
-  const int G = a.Hq / a.Hkv, hpi = a.Hq / a.Hidx;
-  const int n_idx = (G + hpi - 1) / hpi + 1;
+  const int G = a.Hq / a.Hkv;
+  const int n_idx = dec_group_index_heads(a.Hq, a.Hkv, a.Hidx);
   const int mc = dec_max_chunks(n_idx, a.topk_k, a.max_pages);
   const size_t units = size_t(a.T) * a.Hkv * mc * G;
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
@@ -985,8 +994,8 @@ cudaError_t launch_decode(const AttnArgs& a, cudaStream_t stream, const char** w
 size_t attn_workspace_bytes(int B, int T, int max_q_len, int Hq, int Hkv, int Hidx, int topk,
                             int max_pages) {
   if (max_q_len <= 1) {
-    const int G = Hq / Hkv, hpi = Hq / Hidx;
-    const int n_idx = (G + hpi - 1) / hpi + 1;          // index heads one kv group can touch
+    const int G = Hq / Hkv;
+    const int n_idx = dec_group_index_heads(Hq, Hkv, Hidx);   // index heads one kv group reads
     const int mc = dec_max_chunks(n_idx, topk, max_pages);
     const size_t units = size_t(T) * Hkv * mc * G;
     return align256(units * 128 * sizeof(float)) + align256(units * sizeof(DecodePartial)) +
