@@ -93,17 +93,26 @@ def _ptr(t: Optional[torch.Tensor]):
 
 
 def _scale(s: Optional[float]):
-    return None if s is None else ctypes.pointer(ctypes.c_float(float(s)))
+    # a float passed by reference (the C side reads it during the call)
+    return None if s is None else ctypes.byref(ctypes.c_float(float(s)))
 
 
 def _device(*tensors) -> torch.device:
     """The one device every given tensor (None entries skipped) lives on. A
     call whose tensors sit on different GPUs is refused: the library would
     launch on one device with another device's pointers."""
-    devs = {t.device for t in tensors if t is not None}
-    if len(devs) != 1:
-        raise MsaError(1, f"all tensors must be on one device, got {sorted(str(d) for d in devs)}")
-    return next(iter(devs))
+    dev = None
+    for t in tensors:
+        if t is None:
+            continue
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            devs = {str(u.device) for u in tensors if u is not None}
+            raise MsaError(1, f"all tensors must be on one device, got {sorted(devs)}")
+    if dev is None:
+        raise MsaError(1, "no tensor given")
+    return dev
 
 
 _NULL_CTX = contextlib.nullcontext()
@@ -142,7 +151,7 @@ def _dev(t: torch.Tensor, name: str, dtype=None, shape=None) -> None:
         raise MsaError(1, f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
         raise MsaError(1, f"{name} must be contiguous")
-    if shape is not None and tuple(t.shape) != tuple(shape):
+    if shape is not None and t.shape != shape:
         raise MsaError(1, f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
 
 
@@ -213,13 +222,16 @@ def quant_fp8(x: torch.Tensor, scale: Optional[float] = None, out: Optional[torc
 
 
 class _QuantTensor(ctypes.Structure):
-    """msa_quant_tensor of include/msa.h."""
+    """msa_quant_tensor of include/msa.h (scale: a const float*, here as an address)."""
     _fields_ = [("x", ctypes.c_void_p), ("rows", ctypes.c_int64), ("cols", ctypes.c_int64),
                 ("x_row_stride", ctypes.c_int64), ("out", ctypes.c_void_p),
-                ("out_row_stride", ctypes.c_int64), ("scale", ctypes.POINTER(ctypes.c_float))]
+                ("out_row_stride", ctypes.c_int64), ("scale", ctypes.c_void_p)]
 
 
 QUANT_MULTI_MAX = 8
+# array types made once (building a ctypes array type costs more than the call)
+_QT_ARRAYS = [None] + [_QuantTensor * n for n in range(1, QUANT_MULTI_MAX + 1)]
+_F32_ARRAYS = [None] + [ctypes.c_float * n for n in range(1, QUANT_MULTI_MAX + 1)]
 
 
 def quant_fp8_multi(items, stream=None):
@@ -229,13 +241,17 @@ def quant_fp8_multi(items, stream=None):
     dtype for all) and a contiguous last dimension; returns the e4m3 outputs,
     each byte-identical to quant_fp8(x, scale)."""
     lib = load()
-    if not 1 <= len(items) <= QUANT_MULTI_MAX:
-        raise MsaError(1, f"need 1..{QUANT_MULTI_MAX} tensors, got {len(items)}")
+    n_items = len(items)
+    if not 1 <= n_items <= QUANT_MULTI_MAX:
+        raise MsaError(1, f"need 1..{QUANT_MULTI_MAX} tensors, got {n_items}")
     dt = items[0][0].dtype
     if dt not in (torch.bfloat16, torch.float16):
         raise MsaError(1, f"x must be bf16 or fp16, got {dt}")
-    descs = (_QuantTensor * len(items))()
-    keep, outs, tensors = [], [], []
+    descs = _QT_ARRAYS[n_items]()
+    scales = _F32_ARRAYS[n_items]()          # the scales the descriptors point at
+    s_addr = ctypes.addressof(scales)
+    keep, outs = [], []
+    dev = items[0][0].device
     for i, it in enumerate(items):
         x, scale = it[0], it[1]
         out = it[2] if len(it) > 2 else None
@@ -259,14 +275,18 @@ def quant_fp8_multi(items, stream=None):
             _dev(out, "out", torch.uint8)
             if out.numel() != n:
                 raise MsaError(1, f"out must hold {n} elements, got {out.numel()}")
-        sc = _scale(scale)
-        keep.append((x2, sc))
-        descs[i] = _QuantTensor(x2.data_ptr(), rows, cols, xstride, out.data_ptr(), cols, sc)
+        if x.device != dev or out.device != dev:
+            raise MsaError(1, f"all tensors must be on one device, got {x.device} / {out.device} / {dev}")
+        d = descs[i]
+        d.x, d.rows, d.cols, d.x_row_stride = x2.data_ptr(), rows, cols, xstride
+        d.out, d.out_row_stride = out.data_ptr(), cols
+        if scale is not None:
+            scales[i] = float(scale)
+            d.scale = s_addr + 4 * i
+        keep.append(x2)
         outs.append(out)
-        tensors += [x, out]
-    dev = _device(*tensors)
     with _on(dev):
-        _check(lib.msa_quant_fp8_multi(ctypes.cast(descs, ctypes.c_void_p), len(items),
+        _check(lib.msa_quant_fp8_multi(ctypes.addressof(descs), n_items,
                                        MSA_BF16 if dt == torch.bfloat16 else MSA_FP16, MSA_E4M3,
                                        _stream(stream, dev)))
     return outs
@@ -396,8 +416,8 @@ def index_topk(idx_q: torch.Tensor, idx_k_cache: torch.Tensor, page_table: torch
     if out is None:
         out = torch.empty((Hidx, T, topk), dtype=torch.int32, device=idx_q.device)
     _dev(out, "out", torch.int32, (Hidx, T, topk))
-    ws_bytes = index_topk_workspace_size(T, Hidx, max_pages)
-    if workspace is None:
+    if workspace is None:           # (a given workspace's size is checked by the library)
+        ws_bytes = index_topk_workspace_size(T, Hidx, max_pages)
         workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=idx_q.device)
     _dev(workspace, "workspace", torch.uint8)
     dev = _device(idx_q, idx_k_cache, page_table, seq_lens, cu_q, out, workspace)
@@ -463,8 +483,8 @@ def sparse_attn_fwd(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tenso
     _dev(out, "out", torch.bfloat16, (T, Hq, D))
     _dev(max_logit, "max_logit", torch.float32, (T, Hq))
     _dev(lse, "lse", torch.float32, (T, Hq))
-    ws_bytes = sparse_attn_workspace_size(B, T, max_q_len, Hq, Hkv, Hidx, topk, max_pages)
-    if workspace is None:
+    if workspace is None:           # (a given workspace's size is checked by the library)
+        ws_bytes = sparse_attn_workspace_size(B, T, max_q_len, Hq, Hkv, Hidx, topk, max_pages)
         workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
     _dev(workspace, "workspace", torch.uint8)
     dev = _device(q, k_cache, v_cache, page_table, seq_lens, cu_q, topk_indices, sink, out,

@@ -217,3 +217,27 @@ def test_tensors_on_two_devices_are_refused(fake):
     with pytest.raises(bd.MsaError, match="one device"):
         bd.sparse_attn_fwd(q, kc, kc.clone(), pt, sl, cu, ids, None, 0.1, None, None, None, 12)
     assert len(fake.calls) == n
+
+
+def test_quant_multi_marshalling(fake, monkeypatch):
+    import ctypes
+    seen = {}
+
+    def capture(addr, n, x_dtype, out_dtype, stream):      # read the descriptors during the call
+        d = (bd._QuantTensor * n).from_address(addr)
+        seen["d"] = [(t.x, t.rows, t.cols, t.x_row_stride, t.out, t.out_row_stride,
+                      None if t.scale is None else ctypes.c_float.from_address(t.scale).value)
+                     for t in d]
+        seen["n"], seen["dtype"] = n, x_dtype
+        return 0
+    monkeypatch.setattr(fake, "msa_quant_fp8_multi", capture, raising=False)
+    x = torch.zeros((6, 4, 32), dtype=torch.bfloat16)
+    y = torch.zeros((5, 64), dtype=torch.bfloat16)[:, :32]         # row-strided view
+    oy = torch.zeros((5, 32), dtype=torch.uint8)
+    outs = bd.quant_fp8_multi([(x, 0.25), (y, None, oy)])
+    assert outs[1] is oy and tuple(outs[0].shape) == (6, 4, 32)
+    assert seen["n"] == 2 and seen["dtype"] == bd.MSA_BF16
+    assert seen["d"][0] == (x.data_ptr(), 24, 32, 32, outs[0].data_ptr(), 32, 0.25)
+    assert seen["d"][1] == (y.data_ptr(), 5, 32, 64, oy.data_ptr(), 32, None)
+    with pytest.raises(bd.MsaError):                                # mixed dtypes
+        bd.quant_fp8_multi([(x, 1.0), (y.to(torch.float16), 1.0)])
