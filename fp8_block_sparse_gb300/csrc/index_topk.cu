@@ -489,11 +489,14 @@ cudaError_t launch_index_topk(const IndexArgs& a, cudaStream_t stream, const cha
                    n_tiles, a.T, a.Hidx, toks, a.max_pages, a.num_pages, chunks, scores, a.err);
     if (e != cudaSuccess) return e;
   }
+  // one warp per row; few rows (a decode batch) go one warp per CTA so that
+  // they spread over every SM instead of queueing eight to a CTA
   const long long rows = (long long)a.Hidx * a.T;
-  const int grid = int((rows + 7) / 8);
+  const int wpc = rows < 8LL * num_sms() ? 1 : 8;
+  const int grid = int((rows + wpc - 1) / wpc);
   auto sel = a.max_pages <= 256 ? topk_select_kernel<8>
             : a.max_pages <= 512 ? topk_select_kernel<16> : topk_select_kernel<64>;
-  e = launch_pdl(sel, grid, 256, 0, stream, scores, a.seq_lens, a.cu_q, a.B, a.T, a.Hidx, a.topk,
+  e = launch_pdl(sel, grid, 32 * wpc, 0, stream, scores, a.seq_lens, a.cu_q, a.B, a.T, a.Hidx, a.topk,
                  a.max_pages, int(decode), a.topk_indices, a.err);
   profile_mark(stream, 1);
   return e;
