@@ -342,15 +342,20 @@ def mla_measure(msa, wl, dev, steps, flush, pk, only=None):
         step()
     torch.cuda.synchronize()
     ms, kern = [], []
+    msa.profile_enable(False)                  # timed steps as a caller runs them
     for _ in range(steps):
         flush()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         step()
         b.record()
-        kern.append(msa.profile_last_ms())
         torch.cuda.synchronize()
         ms.append(a.elapsed_time(b))
+    msa.profile_enable(True)                   # the MLA kernel alone
+    for _ in range(steps):
+        flush()
+        step()
+        kern.append(msa.profile_last_ms())
     msa.check_errors()
     # the fused producer of the same q: rotary embedding of q[..., 512:] and
     # e4m3 of nope || rope(pe), one launch per step
@@ -670,10 +675,27 @@ def native_arm(args):
     clocks = Clocks(gpu_id)
     clocks.start()
     barrier()
+    # the timed steps run as a caller runs them: no event between the calls
+    # (an event recorded between two launches ends their programmatic
+    # overlap), the library's profile events off
+    msa.profile_enable(False)
+    s = torch.cuda.current_stream()
     for k in range(args.steps):
         flush()
-        s = torch.cuda.current_stream()
         ev[k][0].record(s)
+        run_path(msa, st)
+        ev[k][1].record(s)
+    barrier()
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = world_max(sum(step_ms), world, dev)
+    msa.check_errors()
+
+    # ---- where a step's time goes: the same steps again, with events between
+    # the calls and the library's events around the attention kernel
+    msa.profile_enable(True)
+    for k in range(args.steps):
+        flush()
         c = cuts[k]
         c[0].record(s)
         msa.quant_fp8_multi([(st["q"], st["w"].scales["q"], st["q8"]),
@@ -688,12 +710,7 @@ def native_arm(args):
                             w.max_q_len, out=st["o"], max_logit=st["ml"], lse=st["lse"],
                             workspace=st["ws_attn"])
         c[3].record(s)
-        ev[k][1].record(s)
         attn_ms.append(msa.profile_last_ms())
-    barrier()
-    clk = clocks.stop()
-    step_ms = [a.elapsed_time(b) for a, b in ev]
-    total_ms = world_max(sum(step_ms), world, dev)
     quant_ms = statistics.mean(c[0].elapsed_time(c[1]) for c in cuts)
     index_ms = statistics.mean(c[1].elapsed_time(c[2]) for c in cuts)
     attn_call_ms = statistics.mean(c[2].elapsed_time(c[3]) for c in cuts)
@@ -743,6 +760,7 @@ def native_arm(args):
     h2d = st["q_host"].numel() * 2 + st["iq_host"].numel() * 2
     d2h = st["o_host"].numel() * 2 + st["lse_host"].numel() * 4 + st["ml_host"].numel() * 4
     e2e = None
+    msa.profile_enable(False)          # end to end as a caller runs it
     barrier()
     if not args.no_e2e:
         e2e = _e2e(msa, st, args, world, dev, h2d, d2h, barrier, T)
@@ -760,15 +778,20 @@ def native_arm(args):
             run_path(msa, ds)
         torch.cuda.synchronize()
         d_ms, d_kern = [], []
+        msa.profile_enable(False)                  # timed steps as a caller runs them
         for k in range(args.steps):
             flush()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record()
             run_path(msa, ds)
             b.record()
-            d_kern.append(msa.profile_last_ms())
             torch.cuda.synchronize()
             d_ms.append(a.elapsed_time(b))
+        msa.profile_enable(True)                   # the attention kernel alone
+        for k in range(args.steps):
+            flush()
+            run_path(msa, ds)
+            d_kern.append(msa.profile_last_ms())
         msa.check_errors()
         # the same step captured once as a CUDA graph (quantise -> index top-k
         # -> attention chained without host work between launches) and replayed
