@@ -57,3 +57,45 @@ def test_whole_path_on_its_own_selection(msa, name):
     got = (o.float().cpu().numpy().astype(np.float64), ml.cpu().numpy(), lse.cpu().numpy())
     err, rel = _check(got, ref)
     print(f"{name}: {len(red)} tokens redrawn; O max-abs {err:.2e}, rel-F {rel:.2e}")
+
+
+def test_graph_replay_of_the_path_matches_the_oracle(msa):
+    """The same chain (multi-tensor quantise -> index top-k -> attention, all
+    launched with programmatic dependent launch) captured once as a CUDA
+    graph and replayed: ids bit for bit and O / lse / max_logit against the
+    oracle, on the tiny configuration."""
+    import bench
+    st = bench.gqa_setup(msa, wl, "tiny", torch.device("cuda:0"))
+    w = st["w"]
+    cfg = w.cfg
+    ik_ref = oq.quantize(w.idx_k_pool, w.scales["idx_k"])
+    w.idx_q, red = no_tie.redraw_near_ties(w.idx_q, w.scales["idx_q"], ik_ref, w.page_table,
+                                           w.seq_lens, w.cu_q, cfg.topk, wl.idx_q_redraw(w))
+    st["iq"].copy_(dev_bf16(w.idx_q))
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):                 # warm-up on a side stream before capture
+        bench.run_path(msa, st)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    for k in ("ids", "o", "ml", "lse"):
+        st[k].zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        bench.run_path(msa, st)
+    g.replay()
+    torch.cuda.synchronize()
+    msa.check_errors()
+    q_ref, iq_ref = oq.quantize(w.q, w.scales["q"]), oq.quantize(w.idx_q, w.scales["idx_q"])
+    assert np.array_equal(st["q8"].cpu().numpy(), q_ref)
+    assert np.array_equal(st["iq8"].cpu().numpy(), iq_ref)
+    ids_ref, gaps = oi.index_topk(iq_ref, ik_ref, w.page_table, w.seq_lens, w.cu_q, cfg.topk)
+    assert np.array_equal(st["ids"].cpu().numpy(), ids_ref)
+    ref = oa.sparse_attention(q_ref, oq.quantize(w.k_pool, w.scales["k"]),
+                              oq.quantize(w.v_pool, w.scales["v"]), w.page_table, w.seq_lens,
+                              w.cu_q, ids_ref, w.sink, w.sm_scale, w.scales["q"], w.scales["k"],
+                              w.scales["v"])
+    got = (st["o"].float().cpu().numpy().astype(np.float64), st["ml"].cpu().numpy(),
+           st["lse"].cpu().numpy())
+    err, rel = _check(got, ref)
+    print(f"graph replay: {len(red)} tokens redrawn; O max-abs {err:.2e}, rel-F {rel:.2e}")
