@@ -172,17 +172,32 @@ index_score_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
       sScore[row * kScorePitch + j] = m;
     }
     asm volatile("bar.sync 1, 128;" ::: "memory");
-    // rows -> (token, head): warp e takes rows e, e+4, ..., its lanes write
-    // a row's nblk scores as contiguous words (Hidx is a power of two, so
-    // the row's token and head come from a shift and a mask; a division per
-    // element made this store a quarter of the CTA's time)
+    // rows -> (token, head): warp e takes rows e, e+4, ..., e+124 and lane l
+    // writes columns l and l+32 of each, eight rows at a time with all their
+    // shared-memory reads issued before the first global store (one row per
+    // round trip kept this phase at ~18% of a CTA's life). Hidx is a power
+    // of two, so a row's token and head are a shift and a mask.
+    static_assert(kChunk == 64, "two score columns per lane");
     const int hshift = __ffs(Hidx) - 1;
-    for (int r = warp - 2; r < 128; r += 4) {
-      const int tl = r >> hshift;
-      if (tl >= n_tok) break;                                 // rows are token-major
-      float* dst = scores + (size_t(r & (Hidx - 1)) * T + ti.t0 + tl) * max_pages + c0;
-      const float* src = sScore + r * kScorePitch;
-      for (int jj = lane; jj < nblk; jj += 32) dst[jj] = src[jj];
+    const bool col_lo = lane < nblk, col_hi = lane + 32 < nblk;
+#pragma unroll 1
+    for (int r0 = warp - 2; r0 < 128; r0 += 32) {
+      float v_lo[8], v_hi[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float* src = sScore + (r0 + 4 * k) * kScorePitch;
+        v_lo[k] = src[lane];
+        v_hi[k] = src[lane + 32];
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int r = r0 + 4 * k, tl = r >> hshift;
+        if (tl < n_tok) {                                   // rows past the tile's tokens: none
+          float* dst = scores + (size_t(r & (Hidx - 1)) * T + ti.t0 + tl) * max_pages + c0;
+          if (col_lo) dst[lane] = v_lo[k];
+          if (col_hi) dst[lane + 32] = v_hi[k];
+        }
+      }
     }
   }
   tc_fence_before();
@@ -344,6 +359,7 @@ MSA_DEV void select_row(const float* __restrict__ s, int own, int kp, int lane, 
   const uint32_t diff = kand ^ kor;
   const int top = diff ? 31 - __clz(diff) : -1;            // highest bit that differs
   uint32_t tau = top < 0 ? kand : (top == 31 ? 0u : (kand & ~((2u << top) - 1u)));
+  bool exact = false;
   for (int bit = top; bit >= 0; --bit) {
     const uint32_t tr = tau | (1u << bit);
     int cnt = 0;
@@ -352,15 +368,29 @@ MSA_DEV void select_row(const float* __restrict__ s, int own, int kp, int lane, 
     cnt = __reduce_add_sync(0xffffffffu, cnt);
     if (cnt >= kp) {
       tau = tr;
-      if (cnt == kp) break;                                 // uniform: cnt is warp-wide
+      if (cnt == kp) { exact = true; break; }               // uniform: cnt is warp-wide
     }
+  }
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  if (exact) {
+    // exactly kp keys reach tau (>= 1, so no empty slot among them): no ties
+    // to break, the selection is every key >= tau
+    int pos = 0;
+#pragma unroll
+    for (int r = 0; r < NPL; ++r) {
+      const bool sel = key[r] >= tau;
+      const uint32_t sel_mask = __ballot_sync(0xffffffffu, sel);
+      if (sel) o[pos + __popc(sel_mask & lt_mask)] = r * 32 + lane;
+      pos += __popc(sel_mask);
+    }
+    if (lane == 0) o[kp] = own;
+    return;
   }
   int gt = 0;
 #pragma unroll
   for (int r = 0; r < NPL; ++r) gt += key[r] > tau;
   gt = __reduce_add_sync(0xffffffffu, gt);
   const int need_ties = kp - gt;
-  const uint32_t lt_mask = (1u << lane) - 1u;
   int pos = 0, ties_seen = 0;
 #pragma unroll
   for (int r = 0; r < NPL; ++r) {
@@ -389,15 +419,16 @@ topk_select_kernel(const float* __restrict__ scores, const int32_t* __restrict__
   pdl_wait();      // the scores come from the scoring kernel
   pdl_trigger();
   const int lane = threadIdx.x & 31;
-  const long long row = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (row >= (long long)Hidx * T) return;
-  const int i = int(row / T), t = int(row % T);
+  const int i = blockIdx.y;                                  // index head
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const size_t row = size_t(i) * T + t;
   // with one query per sequence (decode: q_len <= 1, T == B) token t is
   // sequence t; otherwise search the query offsets
   const int b = (decode && T == B) ? t : find_sequence(cu_q, B, t);
   const int qlen = cu_q[b + 1] - cu_q[b], L = seq_lens[b];
   const int p = L - qlen + (t - cu_q[b]);
-  int32_t* o = out + size_t(row) * topk;
+  int32_t* o = out + row * topk;
   // a token outside every sequence, or of a sequence that does not fit its
   // page-table row (the tile plan gives it no scores): a -1 row and a data error
   if (t >= cu_q[b + 1] || qlen < 0 || L < qlen || L > max_pages * 128 || p < 0 ||
@@ -411,7 +442,7 @@ topk_select_kernel(const float* __restrict__ scores, const int32_t* __restrict__
     for (int j = lane; j < topk; j += 32) o[j] = (j <= own) ? j : -1;
     return;
   }
-  const float* s = scores + (size_t(i) * T + t) * max_pages;
+  const float* s = scores + row * max_pages;
   const int kp = topk - 1;
   if (NPL > 2 && own <= 64) select_row<2>(s, own, kp, lane, o);
   else if (NPL > 4 && own <= 128) select_row<4>(s, own, kp, lane, o);
@@ -489,11 +520,12 @@ cudaError_t launch_index_topk(const IndexArgs& a, cudaStream_t stream, const cha
                    n_tiles, a.T, a.Hidx, toks, a.max_pages, a.num_pages, chunks, scores, a.err);
     if (e != cudaSuccess) return e;
   }
-  // one warp per row; few rows (a decode batch) go one warp per CTA so that
-  // they spread over every SM instead of queueing eight to a CTA
+  // one warp per row, grid (tokens, index heads); few rows (a decode batch)
+  // go one warp per CTA so that they spread over every SM instead of
+  // queueing eight to a CTA
   const long long rows = (long long)a.Hidx * a.T;
   const int wpc = rows < 8LL * num_sms() ? 1 : 8;
-  const int grid = int((rows + wpc - 1) / wpc);
+  const dim3 grid(unsigned((a.T + wpc - 1) / wpc), unsigned(a.Hidx));
   auto sel = a.max_pages <= 256 ? topk_select_kernel<8>
             : a.max_pages <= 512 ? topk_select_kernel<16> : topk_select_kernel<64>;
   e = launch_pdl(sel, grid, 32 * wpc, 0, stream, scores, a.seq_lens, a.cu_q, a.B, a.T, a.Hidx, a.topk,
