@@ -15,17 +15,21 @@
 //   3-stage TMA ring. Each page is one M=128 x N=128 x K=D e4m3 MMA into a
 //   double-buffered TMEM accumulator; four epilogue warps read their rows out
 //   of TMEM and reduce the 128 columns to the block maximum. Scores of a
-//   64-block chunk are staged in shared memory and written as contiguous rows.
+//   64-block chunk are staged in shared memory; a full tile's go out by TMA
+//   (boxes of [Hidx][tokens][32 blocks]), a ragged tile's by its threads.
 // * Decode (one query token per sequence) is a stream over the index-K pages;
 //   it runs the same MMA with the roles swapped (M=128 keys of the page,
 //   N=16 query columns of which Hidx are used) so the page is the A operand
 //   straight out of the TMA ring and the max runs across TMEM lanes.
-// * Selection is one warp per row: a 32-step radix select finds the
-//   (topk-1)-th largest score bit-exactly on the fp32 key, then ballot/popc
-//   writes the chosen ids in ascending order.
+// * Selection is one warp per row: a radix select over the bits of the
+//   order-preserving fp32 key finds the (topk-1)-th largest score exactly,
+//   then ballot/popc writes the chosen ids in ascending order (a row whose
+//   threshold has exactly topk-1 keys at or above it needs no tie pass).
 #include "common.cuh"
 #include "internal.h"
 #include "plan.cuh"
+
+#include <cstring>
 
 namespace msa {
 namespace {
@@ -49,7 +53,9 @@ template <int D>
 struct PrefillSmem {
   static constexpr int kQ = 0;                               // 128 x D
   static constexpr int kK = 16384;                           // kStages x (128 x D)
-  static constexpr int kScore = kK + kStages * 16384;        // 128 x kScorePitch fp32
+  // 128 x kScorePitch fp32, or (full tiles, TMA store) two 16 KB boxes of
+  // [Hidx][tokens][32 columns] in the 128-byte swizzle
+  static constexpr int kScore = kK + kStages * 16384;
   static constexpr int kBytes = kScore + 128 * kScorePitch * 4 + 1024;   // + alignment slack
 };
 
@@ -59,6 +65,7 @@ template <int D>
 __global__ void __maxnreg__(128)
 index_score_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                            const __grid_constant__ CUtensorMap tm_k,
+                           const __grid_constant__ CUtensorMap tm_s, int tma_store,
                            const int32_t* __restrict__ page_table,
                            const TileInfo* __restrict__ tiles, const int* __restrict__ n_tiles_p,
                            int T, int Hidx, int toks, int max_pages, int num_pages,
@@ -84,6 +91,9 @@ index_score_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
   const int c0 = (blockIdx.x % chunks_per_tile) * kChunk;
   if (c0 >= nb) return;
   const int nblk = min(kChunk, nb - c0);
+  // a full tile's rows go out by TMA (ragged tiles must not touch the rows
+  // of the next sequence's tokens, which the box would cover)
+  const bool via_tma = tma_store && n_tok == toks;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   uint8_t* sQ = smem + L::kQ;
@@ -145,6 +155,11 @@ index_score_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
   } else {
     // epilogue: warps 2..5 own TMEM lanes 32*(warp%4) .. +31
     const int row = (warp & 3) * 32 + lane;
+    const int hshift = __ffs(Hidx) - 1;      // Hidx is a power of two
+    // box row of this TMEM row (token-major -> head-major) and its 16-byte
+    // chunk swizzle
+    const int brow = (row & (Hidx - 1)) * toks + (row >> hshift);
+    float* bdst = sScore + brow * 32;
     for (int j = 0; j < nblk; ++j) {
       const int buf = j & 1;
       if (!mbar_wait_warp(&bar_tfull[buf], (j >> 1) & 1, err, &abort_s)) break;   // uniform
@@ -169,33 +184,49 @@ index_score_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_tempty[buf]);
-      sScore[row * kScorePitch + j] = m;
-    }
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-    // rows -> (token, head): warp e takes rows e, e+4, ..., e+124 and lane l
-    // writes columns l and l+32 of each, eight rows at a time with all their
-    // shared-memory reads issued before the first global store (one row per
-    // round trip kept this phase at ~18% of a CTA's life). Hidx is a power
-    // of two, so a row's token and head are a shift and a mask.
-    static_assert(kChunk == 64, "two score columns per lane");
-    const int hshift = __ffs(Hidx) - 1;
-    const bool col_lo = lane < nblk, col_hi = lane + 32 < nblk;
-#pragma unroll 1
-    for (int r0 = warp - 2; r0 < 128; r0 += 32) {
-      float v_lo[8], v_hi[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const float* src = sScore + (r0 + 4 * k) * kScorePitch;
-        v_lo[k] = src[lane];
-        v_hi[k] = src[lane + 32];
+      if (via_tma) {
+        const int c = j & 31;
+        bdst[(j >> 5) * 4096 + ((((c >> 2) ^ (brow & 7)) << 2) | (c & 3))] = m;
+      } else {
+        sScore[row * kScorePitch + j] = m;
       }
+    }
+    if (via_tma) {
+      fence_async_shared();                  // score writes -> the TMA store's reads
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      if (tid == 64) {
+        // columns past nblk are blocks no token of the tile selects from
+        tma_store_3d(&tm_s, sScore, c0, ti.t0, 0);
+        if (nblk > 32) tma_store_3d(&tm_s, sScore + 4096, c0 + 32, ti.t0, 0);
+        bulk_commit();
+        bulk_wait_read();                    // shared memory stays until read
+      }
+    } else {
+      asm volatile("bar.sync 1, 128;" ::: "memory");
+      // rows -> (token, head): warp e takes rows e, e+4, ..., e+124 and lane l
+      // writes columns l and l+32 of each, eight rows at a time with all their
+      // shared-memory reads issued before the first global store (one row per
+      // round trip kept this phase at ~18% of a CTA's life). Hidx is a power
+      // of two, so a row's token and head are a shift and a mask.
+      static_assert(kChunk == 64, "two score columns per lane");
+      const bool col_lo = lane < nblk, col_hi = lane + 32 < nblk;
+#pragma unroll 1
+      for (int r0 = warp - 2; r0 < 128; r0 += 32) {
+        float v_lo[8], v_hi[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int r = r0 + 4 * k, tl = r >> hshift;
-        if (tl < n_tok) {                                   // rows past the tile's tokens: none
-          float* dst = scores + (size_t(r & (Hidx - 1)) * T + ti.t0 + tl) * max_pages + c0;
-          if (col_lo) dst[lane] = v_lo[k];
-          if (col_hi) dst[lane + 32] = v_hi[k];
+        for (int k = 0; k < 8; ++k) {
+          const float* src = sScore + (r0 + 4 * k) * kScorePitch;
+          v_lo[k] = src[lane];
+          v_hi[k] = src[lane + 32];
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int r = r0 + 4 * k, tl = r >> hshift;
+          if (tl < n_tok) {                                   // rows past the tile's tokens: none
+            float* dst = scores + (size_t(r & (Hidx - 1)) * T + ti.t0 + tl) * max_pages + c0;
+            if (col_lo) dst[lane] = v_lo[k];
+            if (col_hi) dst[lane + 32] = v_hi[k];
+          }
         }
       }
     }
@@ -516,7 +547,23 @@ cudaError_t launch_index_topk(const IndexArgs& a, cudaStream_t stream, const cha
     if (e != cudaSuccess) return e;
     const int n_tiles_max = (a.T + toks - 1) / toks + a.B;
     profile_mark(stream, 0);
-    e = launch_pdl(kern, n_tiles_max * chunks, 192, smem, stream, tm_q, tm_k, a.page_table, tiles,
+    // scores as [Hidx][T][max_pages] fp32 for the TMA store of full tiles
+    // (row pitch a multiple of 16 bytes, else every tile stores by threads)
+    CUtensorMap tm_s;
+    int tma_store = 0;
+    if (a.max_pages % 4 == 0) {
+      const uint64_t dims[3] = {uint64_t(a.max_pages), uint64_t(a.T), uint64_t(a.Hidx)};
+      const uint64_t strides[2] = {uint64_t(a.max_pages) * 4, uint64_t(a.T) * a.max_pages * 4};
+      const uint32_t box[3] = {32u, uint32_t(toks), uint32_t(a.Hidx)};
+      if (!encode_tensor_map(&tm_s, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, scores, dims, strides, box,
+                             CU_TENSOR_MAP_SWIZZLE_128B, why))
+        return cudaErrorInvalidValue;
+      tma_store = 1;
+    } else {
+      std::memset(&tm_s, 0, sizeof(tm_s));
+    }
+    e = launch_pdl(kern, n_tiles_max * chunks, 192, smem, stream, tm_q, tm_k, tm_s, tma_store,
+                   a.page_table, tiles,
                    n_tiles, a.T, a.Hidx, toks, a.max_pages, a.num_pages, chunks, scores, a.err);
     if (e != cudaSuccess) return e;
   }

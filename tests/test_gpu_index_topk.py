@@ -74,10 +74,14 @@ def test_prefill32k_sampled(msa):
     _run(msa, w, tokens=sample_tokens(w.T, 256, 1))
 
 
-def test_varlen_prefill_with_prefix(msa):
-    # three sequences, the last two continue an existing prefix (q_len < seq_len)
-    cfg = wl.GQAConfig("varlen", 3, (700, 1500, 2100), 0, 16, 2, 4, 128, 128, 8, "channel",
-                       pool_factor=1.2, seed=11)
+@pytest.mark.parametrize("Hidx,max_pages", [(4, 0), (4, 20), (8, 24), (2, 32)])
+def test_varlen_prefill_with_prefix(msa, Hidx, max_pages):
+    # three sequences, the last two continue an existing prefix (q_len < seq_len);
+    # with a page-table width that is a multiple of 4 the full query tiles write
+    # their scores by TMA and the ragged ones (each sequence's last) by threads,
+    # next to the rows of the following sequence's tokens
+    cfg = wl.GQAConfig("varlen", 3, (700, 1500, 2100), 0, 16, 2, Hidx, 128, 128, 8, "channel",
+                       max_pages=max_pages, pool_factor=1.2, seed=11)
     w = wl.make_gqa(cfg)
     q_lens = np.array([700, 300, 257], np.int32)
     w.cu_q = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int32)
