@@ -162,12 +162,6 @@ MSA_DEV void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y)
       ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(src)), "r"(x), "r"(y)
       : "memory");
 }
-MSA_DEV void tma_store_3d(const CUtensorMap* map, const void* src, int x, int y, int z) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];"
-      ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(src)), "r"(x), "r"(y), "r"(z)
-      : "memory");
-}
 MSA_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 MSA_DEV void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 // Plain bulk copy global -> shared (both 16-byte aligned, size a multiple of 16).

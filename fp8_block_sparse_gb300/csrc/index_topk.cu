@@ -38,6 +38,14 @@ constexpr int kChunk = 64;       // blocks scored per CTA (64 measured 7% faster
 constexpr int kStages = 3;       // TMA ring depth (3 keeps two CTAs per SM with 64-block chunks)
 constexpr int kScorePitch = kChunk + 1;
 
+// Tiled TMA store of one 3-D box from shared memory (bulk-group completion).
+MSA_DEV void tma_store_3d(const CUtensorMap* map, const void* src, int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];"
+      ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(src)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
 // Order-preserving map of fp32 onto uint32 (larger float -> larger key).
 MSA_DEV uint32_t order_key(float x) {
   uint32_t u = __float_as_uint(x);

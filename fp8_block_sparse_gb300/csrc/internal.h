@@ -131,7 +131,6 @@ struct IndexArgs {
   int B, T, max_q_len, Hidx, D, topk, num_pages, max_pages;
   int32_t* topk_indices;
   float* scores;
-  int32_t* tile_map;   // workspace: per-CTA (sequence, first token) list for prefill tiles
   unsigned* err;
 };
 cudaError_t launch_index_topk(const IndexArgs& a, cudaStream_t stream, const char** why);
