@@ -15,10 +15,10 @@
 // Host code cannot use the array's name as a device address (in host code it
 // names a host-side stand-in), so the device address is looked up with
 // cudaGetSymbolAddress once per device, with that device current, on the
-// first call made on that device; make that first call before any stream
-// capture. All calls share the one array and it keeps the last call's
-// contents; calls whose work overlaps on the GPU (different streams without
-// ordering between them) race on it and must be serialised by the caller.
+// first call made on that device. All calls share the one array and it keeps
+// the last call's contents; calls whose work overlaps on the GPU (different
+// streams without ordering between them) race on it and must be serialised
+// by the caller.
 // Nothing in it needs to start at zero: every entry a call reads was written
 // earlier by the same call.
 #include <mutex>

@@ -309,8 +309,7 @@ msa_status msa_index_topk(const uint8_t* idx_q, const uint8_t* idx_k_cache,
  *   paged-decode workload (128 sequences x 4 index heads x 512 pages, 1 MiB)
  *   and short prefills fit, long prefills need msa_index_topk.
  * - The first call on a device looks up the array's device address
- *   (cudaGetSymbolAddress, with that device current); make that first call
- *   before any stream capture.
+ *   (cudaGetSymbolAddress, with that device current).
  * - Every call uses the same array and leaves its contents behind; calls
  *   that may run at the same time on the GPU (unordered streams) race on it
  *   and must be serialised by the caller. No contents need to start at zero.
