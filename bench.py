@@ -159,6 +159,25 @@ def traffic_for(kernel_file: str, profile_name: str):
         return None
 
 
+def _queued_ms(fn, steps, flush):
+    """Device milliseconds of each of `steps` calls of `fn`, queued back to
+    back on the current stream (flush, event, call, event) with one
+    synchronisation after the last: the host's launches run ahead of the GPU
+    as in a serving loop, where a synchronisation per step would add the
+    host's launch latency to every step."""
+    import torch
+    s = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for a, b in ev:
+        flush()
+        a.record(s)
+        fn()
+        b.record(s)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
 class L2Flush:
     """Evicts the 129 MB L2 before a timed step: a 256 MB write, then a
     256 MB read, so that the lines left in L2 are clean and the step does not
@@ -341,16 +360,9 @@ def mla_measure(msa, wl, dev, steps, flush, pk, only=None):
     for _ in range(3):
         step()
     torch.cuda.synchronize()
-    ms, kern = [], []
-    msa.profile_enable(False)                  # timed steps as a caller runs them
-    for _ in range(steps):
-        flush()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        step()
-        b.record()
-        torch.cuda.synchronize()
-        ms.append(a.elapsed_time(b))
+    kern = []
+    msa.profile_enable(False)                  # timed steps as a caller runs them, queued
+    ms = _queued_ms(step, steps, flush)
     msa.profile_enable(True)                   # the MLA kernel alone
     for _ in range(steps):
         flush()
@@ -362,15 +374,7 @@ def mla_measure(msa, wl, dev, steps, flush, pk, only=None):
     for _ in range(3):
         rq()
     torch.cuda.synchronize()
-    r_ms = []
-    for _ in range(steps):
-        flush()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        rq()
-        b.record()
-        torch.cuda.synchronize()
-        r_ms.append(a.elapsed_time(b))
+    r_ms = _queued_ms(rq, steps, flush)
     msa.check_errors()
     r_bytes = 3 * q.numel() + 4 * T * (64 + 1)
     rm = statistics.mean(r_ms)
@@ -419,15 +423,7 @@ def kv_store_measure(msa, w, dev, steps, flush, pk, only=None):
     for _ in range(3):
         step()
     torch.cuda.synchronize()
-    ms = []
-    for _ in range(steps):
-        flush()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        step()
-        b.record()
-        torch.cuda.synchronize()
-        ms.append(a.elapsed_time(b))
+    ms = _queued_ms(step, steps, flush)
     msa.check_errors()
     # algorithmic bytes: 2 B read + 1 B written per element, plus the batch description
     elems = T * (2 * c.Hkv * c.D + c.d_idx)
@@ -777,16 +773,9 @@ def native_arm(args):
         for _ in range(3):
             run_path(msa, ds)
         torch.cuda.synchronize()
-        d_ms, d_kern = [], []
-        msa.profile_enable(False)                  # timed steps as a caller runs them
-        for k in range(args.steps):
-            flush()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            run_path(msa, ds)
-            b.record()
-            torch.cuda.synchronize()
-            d_ms.append(a.elapsed_time(b))
+        d_kern = []
+        msa.profile_enable(False)                  # timed steps as a caller runs them, queued
+        d_ms = _queued_ms(lambda: run_path(msa, ds), args.steps, flush)
         msa.profile_enable(True)                   # the attention kernel alone
         for k in range(args.steps):
             flush()
@@ -808,15 +797,7 @@ def native_arm(args):
         for _ in range(3):
             graph.replay()
         torch.cuda.synchronize()
-        g_ms = []
-        for k in range(args.steps):
-            flush()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            graph.replay()
-            b.record()
-            torch.cuda.synchronize()
-            g_ms.append(a.elapsed_time(b))
+        g_ms = _queued_ms(graph.replay, args.steps, flush)
         msa.check_errors()
         del graph
         msa.profile_enable(True)
