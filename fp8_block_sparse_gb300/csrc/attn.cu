@@ -337,15 +337,18 @@ attn_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         uint32_t v[64];
         tmem_ld64(s_col, v);                                  // one round trip
         if (nc == 64) {
+          // columns 0-3 seed four chains, 4-59 in steps of eight, 60-63 last
           float a0 = __uint_as_float(v[0]), a1 = __uint_as_float(v[1]);
           float a2 = __uint_as_float(v[2]), a3 = __uint_as_float(v[3]);
 #pragma unroll
-          for (int c = 4; c < 64; c += 8) {
+          for (int c = 4; c < 60; c += 8) {
             a0 = fmax3(a0, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
             a1 = fmax3(a1, __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
             a2 = fmax3(a2, __uint_as_float(v[c + 4]), __uint_as_float(v[c + 5]));
             a3 = fmax3(a3, __uint_as_float(v[c + 6]), __uint_as_float(v[c + 7]));
           }
+          a0 = fmax3(a0, __uint_as_float(v[60]), __uint_as_float(v[61]));
+          a1 = fmax3(a1, __uint_as_float(v[62]), __uint_as_float(v[63]));
           mr = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
         } else if (nc > 0) {
 #pragma unroll
