@@ -18,7 +18,7 @@ index head selected (topk_indices, strictly ascending with -1 padding, as in
 the vLLM PR 45892 page, step 2: attention reads the buffer the indexer
 wrote), restricted to keys at positions <= the query's position.
 
-Readings where the pages are silent (each listed in the design doc):
+Readings where the pages are silent:
 
 * q head h reads kv head h // (Hq/Hkv) (standard GQA grouping) and index head
   h // (Hq/Hidx);

@@ -18,7 +18,7 @@ What is computed, and where the pages say so:
   written strictly ascending; when a query has no more causal blocks than
   topk, the output is all of them followed by -1 padding.
 
-Readings where the pages are silent (each listed in the design doc):
+Readings where the pages are silent:
 
 * the query's own block (the one holding its position) is always selected and
   takes one of the ``topk`` slots; the other ``topk - 1`` are the highest

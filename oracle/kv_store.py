@@ -14,7 +14,7 @@ What is computed, and where the pages say so:
 * vLLM PR 45892 page, implementation step 3: the index-K cache has no head
   axis, one row of ``d_idx`` codes per token slot.
 
-Readings where the pages are silent (each listed in the design doc):
+Readings where the pages are silent:
 
 * the stored code of an element is the path's quantiser rule,
   ``e4m3(fp32(x) * fp32(1 / scale))``, the same rule as the query

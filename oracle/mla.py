@@ -15,7 +15,7 @@ The scale rules are those of the GQA path (sglang PR 30971 page, step 3):
 q_scale multiplies the dot and the sink, kv_scale multiplies the dot (as the
 k scale) and the output (as the v scale).
 
-Readings where the pages are silent (each listed in the design doc): the first
+Readings where the pages are silent: the first
 topk_length[t] entries of a query's index row are its keys (all topk entries
 when topk_length is absent); entries that are negative are skipped; max_logit
 and lse follow the GQA definitions (sink excluded from max_logit, included in

@@ -15,7 +15,7 @@ What is computed, and where the pages say so:
 * Same page, key source excerpt of ``fp8_quantize``: values are widened to
   fp32, scaled and cast to e4m3.
 
-Readings where the pages are silent (each listed in the design doc):
+Readings where the pages are silent:
 
 * ``cos_sin_cache[pos]`` holds the d_rope/2 cosines followed by the d_rope/2
   sines of that position's angles.
