@@ -118,6 +118,52 @@ def test_decode_config_sampled(msa):
     print(f"decode: {gaps.size} rows exact, {len(red)} of {len(seqs)} sequences redrawn")
 
 
+@pytest.mark.parametrize("kind", ["prefill", "decode"])
+def test_exact_ties_go_to_the_lower_block_id(msa, kind):
+    """Logical blocks that share a physical index-K page score exactly alike
+    on both sides (the same fp32 MMA of the same operands on the GPU, the same
+    exact dot in the oracle), so the selection's tie rule decides: equal
+    scores go to the lower block id (oracle/index_topk.py, reading: ties by
+    the lower id). Every sequence's blocks cycle through three pages; rows
+    whose boundary falls inside a group of equal scores take the tie pass,
+    the others the exact-threshold path. The three pages' exact scores are
+    checked to lie further apart than the fp32 bound of each row, so every
+    row has exactly one correct answer."""
+    if kind == "prefill":
+        w = wl.make_gqa(wl.CONFIGS["tiny"])
+    else:
+        cfg = wl.GQAConfig("dec", 24, (), 1, 16, 2, 4, 128, 128, 8, "channel",
+                           len_range=(1200, 3000), max_pages=24, pool_factor=1.3, seed=21)
+        w = wl.make_gqa(cfg)
+    pt = w.page_table.copy()
+    cols = np.broadcast_to(np.arange(pt.shape[1], dtype=np.int32), pt.shape)
+    pt[pt >= 0] = cols[pt >= 0] % 3
+    ik = oq.quantize(w.idx_k_pool, w.scales["idx_k"])
+    iq = oq.quantize(w.idx_q, w.scales["idx_q"])
+    topk = w.cfg.topk
+    ids = msa.index_topk(dev(iq), dev(ik), dev(pt), dev(w.seq_lens), dev(w.cu_q), topk,
+                         w.max_q_len)
+    msa.check_errors()
+    ref, _ = oi.index_topk(iq, ik, pt, w.seq_lens, w.cu_q, topk)
+    _, pos = oi.query_positions(w.seq_lens, w.cu_q)
+    chooses = np.nonzero(pos // 128 + 1 > topk)[0]             # rows with a choice to make
+    assert chooses.size > 0
+    bound = no_tie.row_bounds(iq, ik, pt, w.seq_lens, w.cu_q, chooses)
+    ties = 0
+    for n, t in enumerate(chooses):
+        sc = oi.block_scores(iq[t], ik, np.arange(3))              # [Hidx, 3]
+        srt = np.sort(sc, axis=1)
+        assert np.all(np.diff(srt, axis=1) > bound[:, n:n + 1]), t
+        own = int(pos[t]) // 128
+        for i in range(sc.shape[0]):
+            per_block = sc[i, np.arange(own) % 3]
+            kth = np.sort(per_block)[::-1][topk - 2:topk]       # the (topk-1)-th and next score
+            ties += int(kth[0] == kth[1])
+    assert ties > 0                                            # the tie pass did run
+    assert np.array_equal(ids.cpu().numpy(), ref)
+    print(f"{kind}: {chooses.size} tokens with a choice, {ties} rows tied at the boundary")
+
+
 def test_bad_page_id_is_reported_not_trapped(msa):
     w = wl.make_gqa(wl.CONFIGS["tiny"], T_override=600)
     w.page_table = w.page_table.copy()
