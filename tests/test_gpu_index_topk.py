@@ -74,7 +74,7 @@ def test_prefill32k_sampled(msa):
     _run(msa, w, tokens=sample_tokens(w.T, 256, 1))
 
 
-@pytest.mark.parametrize("Hidx,max_pages", [(4, 0), (4, 20), (8, 24), (2, 32)])
+@pytest.mark.parametrize("Hidx,max_pages", [(4, 0), (4, 20), (8, 24), (2, 32), (16, 24), (1, 28)])
 def test_varlen_prefill_with_prefix(msa, Hidx, max_pages):
     # three sequences, the last two continue an existing prefix (q_len < seq_len);
     # with a page-table width that is a multiple of 4 the full query tiles write
@@ -93,6 +93,16 @@ def test_varlen_prefill_with_prefix(msa, Hidx, max_pages):
 def test_decode_small_contexts(msa):
     cfg = wl.GQAConfig("dec", 40, (), 1, 16, 2, 4, 128, 128, 8, "channel",
                        len_range=(1, 3000), max_pages=24, pool_factor=1.3, seed=12)
+    _run(msa, wl.make_gqa(cfg))
+
+
+@pytest.mark.parametrize("Hidx,d_idx", [(1, 128), (2, 64), (16, 128)])
+def test_decode_index_head_counts(msa, Hidx, d_idx):
+    # the decode scorer puts a token's Hidx query rows in the N = 16 columns
+    # of one MMA: one column, two, and all sixteen; d_idx 64 takes the 64-byte
+    # swizzle
+    cfg = wl.GQAConfig("dech", 24, (), 1, 16, 1, Hidx, 128, d_idx, 8, "channel",
+                       len_range=(1000, 5000), max_pages=40, pool_factor=1.3, seed=30 + Hidx)
     _run(msa, wl.make_gqa(cfg))
 
 
